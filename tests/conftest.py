@@ -17,5 +17,8 @@ def pytest_configure(config):
 def lib():
     """The product binding with its shared library loaded (fails loudly if not built)."""
     import tiled_distributed_attention_gb300 as m
+    if not os.path.exists(m.LIB_PATH):
+        from tiled_distributed_attention_gb300 import _build
+        _build.build()
     m.load_library()
     return m

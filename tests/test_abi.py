@@ -1,0 +1,168 @@
+"""CPU tests of the C ABI: the library loads, exports every declared entry point, the C++
+planner matches the plain-Python planner oracle bit for bit, and host-side validation
+returns the documented status codes before touching the GPU."""
+import ctypes
+import itertools
+import json
+import math
+import os
+import re
+
+import pytest
+
+from oracle import planner as PL
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mesh_attn.h")
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mesh_attn_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 15
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for n in names:
+        assert hasattr(so, n), f"{n} declared in mesh_attn.h but not exported"
+    assert set(names) == set(lib._SIGS), "binding and header disagree"
+
+
+def cpp_plan(lib, S, P, causal, kvr, greedy):
+    p = lib.mesh_attn_plan_create(S, P, causal, kvr, greedy)
+    q, kv = lib.mesh_attn_plan_tiles(p)
+    off = lib.mesh_attn_plan_slots(p)
+    items, steps, kvs = lib.mesh_attn_plan_order(p)
+    counts, _, _ = lib.mesh_attn_plan_volumes(p, 1, 1, 1)
+    return p, q, kv, off, items, steps, kvs, counts
+
+
+@pytest.mark.parametrize("P", [1, 4, 9, 16, 25, 64, 256])
+@pytest.mark.parametrize("causal,kvr,greedy", list(itertools.product([0, 1], repeat=3)))
+def test_planner_matches_oracle(lib, P, causal, kvr, greedy):
+    S = P * 3
+    ref = PL.make_plan(S, P, bool(causal), bool(kvr), bool(greedy))
+    p, q, kv, off, items, steps, kvs, counts = cpp_plan(lib, S, P, causal, kvr, greedy)
+    assert q == ref.q_parts and kv == ref.kv_parts
+    assert off == ref.slot_off
+    assert [list(i) for i in items] == [list(i) for i in ref.items]
+    assert steps == ref.item_step
+    assert kvs == ref.item_kv
+    assert [list(c) for c in counts] == [list(r) for r in ref.recv]
+    assert p.n_live_blocks == ref.n_live_blocks
+    assert p.n_kv_entries == ref.n_live_blocks
+    assert p.L == 3 and p.R == math.isqrt(P)
+
+
+@pytest.mark.parametrize("name", ["plan_p4_causal_kvr_greedy.json", "plan_p4_causal_nokvr_rowmajor.json"])
+def test_hand_worked_plan_cpp(lib, name):
+    g = json.load(open(os.path.join(GOLDEN, name)))
+    p, q, kv, off, items, steps, kvs, counts = cpp_plan(lib, g["S"], g["P"], g["causal"], g["kvr"], g["greedy"])
+    assert q == g["q_parts"] and kv == g["kv_parts"] and off == g["slot_off"]
+    assert [list(i) for i in items] == g["items"]
+    assert kvs == g["item_kv"] and steps == g["item_step"]
+    assert [list(c) for c in counts] == g["recv"]
+
+
+@pytest.mark.parametrize("row", json.load(open(os.path.join(GOLDEN, "plan_counts.json")))["rows"],
+                         ids=lambda r: r["name"])
+def test_workload_counts_cpp(lib, row):
+    P, causal = row["P"], row["causal"]
+    R = math.isqrt(P)
+    a = lib.mesh_attn_plan_create(P * 256, P, causal, True, True)
+    b = lib.mesh_attn_plan_create(P * 256, P, causal, False, True)
+    assert a.n_slots == row["slots_kvr"] and b.n_slots == row["slots_nokvr"]
+    assert a.n_live_blocks == row["live_blocks"]
+    items_b, _, _ = lib.mesh_attn_plan_order(b)
+    assert P - len({t for _, t, _ in items_b}) == row["idle_nokvr"]
+    counts, _, ring = lib.mesh_attn_plan_volumes(a, 1, 1, 1)
+    assert tuple(max(c[i] for c in counts) for i in range(3)) == (R - 1, R - 1, R - 1)
+
+
+def test_volume_bytes_match_oracle(lib):
+    for causal in (False, True):
+        ref = PL.make_plan(16384, 16, causal, True, True)
+        per, ring = PL.volume_bytes(ref, 16, 16, 128, 2)
+        p = lib.mesh_attn_plan_create(16384, 16, causal, True, True)
+        _, byts, ring_c = lib.mesh_attn_plan_volumes(p, 16, 16, 128)
+        assert [tuple(b) for b in byts] == [tuple(x) for x in per]
+        assert ring_c == ring
+
+
+def test_planner_large_p_consistency(lib):
+    """P = 1024 (the stress workload): slot closed form, coverage of live blocks, order is a
+    permutation of the slots, and each item's KV list lies in its tile's mesh column."""
+    P, R = 1024, 32
+    p = lib.mesh_attn_plan_create(P * 256, P, True, True, True)
+    items, steps, kvs = lib.mesh_attn_plan_order(p)
+    assert p.n_slots == sum(min(x + 1, R) for x in range(P))
+    assert sorted(s for _, _, s in items) == list(range(p.n_slots))
+    assert sum(len(k) for k in kvs) == P * (P + 1) // 2
+    assert steps == sorted(steps)
+    for (q, t, _), kl in zip(items, kvs):
+        assert all(k % R == t % R and k <= q for k in kl)
+
+
+def test_status_codes(lib):
+    so = lib._lib
+    h = ctypes.c_void_p()
+    assert so.mesh_attn_plan_create(100, 8, 1, 1, 1, ctypes.byref(h)) == 1  # P not a square
+    assert "square" in so.mesh_attn_last_error().decode()
+    assert so.mesh_attn_plan_create(10, 4, 1, 1, 1, ctypes.byref(h)) == 1  # S % P
+    assert so.mesh_attn_plan_create(16, 4, 2, 1, 1, ctypes.byref(h)) == 1  # flag not 0/1
+    assert so.mesh_attn_plan_create(16, 0, 1, 1, 1, ctypes.byref(h)) == 1
+    assert so.mesh_attn_plan_create(-4, 4, 1, 1, 1, ctypes.byref(h)) == 1
+    assert so.mesh_attn_plan_create(16 * 4225, 4225, 1, 1, 1, ctypes.byref(h)) == 1  # P > 4096
+    assert so.mesh_attn_plan_create(16, 4, 1, 1, 1, None) == 1
+    plan = lib.mesh_attn_plan_create(1024, 4, True)
+    ws = lib.mesh_attn_workspace_size(plan)
+    fake = ctypes.c_void_p(1 << 20)
+    args = lambda **kw: dict(dict(plan=plan.handle, dt=1, B=1, Hq=2, Hkv=1, d=128, Q=fake, K=fake, V=fake,
+                                  scale=0.1, po=fake, pl=fake, ws=fake, wsb=ws, st=fake, stream=None), **kw)
+
+    def call(**kw):
+        a = args(**kw)
+        return so.mesh_attn_tile_fwd(a["plan"], a["dt"], a["B"], a["Hq"], a["Hkv"], a["d"], a["Q"], a["K"], a["V"],
+                                     a["scale"], a["po"], a["pl"], a["ws"], a["wsb"], a["st"], a["stream"])
+
+    assert call(plan=None) == 1
+    assert call(d=96) == 2
+    assert call(Hkv=3) == 1
+    assert call(dt=7) == 1
+    assert call(scale=0.0) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(Q=None) == 1
+    assert call(K=ctypes.c_void_p((1 << 20) + 8)) == 3
+    assert call(wsb=ws - 1) == 9
+    assert call(B=-1) == 1
+    assert call(B=0) == 0 and call(Hq=0) == 0  # nothing to do: no launch, no CUDA call
+    assert call(B=1 << 20, Hq=1 << 10) == 2    # rows beyond 32-bit coordinates
+    # merge validation
+    assert so.mesh_attn_merge(plan.handle, 5, 1, 2, 128, fake, fake, fake, fake, fake, ws, fake, None) == 1
+    assert so.mesh_attn_merge(plan.handle, 1, 1, 2, 128, fake, fake, fake, fake, fake, ws - 1, fake, None) == 9
+    assert so.mesh_attn_merge(plan.handle, 1, 1, 2, 100, fake, fake, fake, fake, fake, ws, fake, None) == 2
+    assert so.mesh_attn_set_wait_limit_ns(-1) == 1
+    for c in range(10):
+        assert so.mesh_attn_status_string(c)
+    assert so.mesh_attn_plan_destroy(None) == 0
+
+
+def test_empty_sequence_plan(lib):
+    p = lib.mesh_attn_plan_create(0, 16, True)
+    assert p.n_slots == 0 and p.n_live_blocks == 0 and p.L == 0
+    assert lib.mesh_attn_partials_size(p, 2, 4, 128) == (0, 0)
+    # an empty plan enqueues nothing: NULL tensors are accepted
+    rc = lib._lib.mesh_attn_tile_fwd(p.handle, 1, 1, 2, 1, 128, None, None, None, 0.1, None, None, None, 0, None, None)
+    assert rc == 0
+    rc = lib._lib.mesh_attn_merge(p.handle, 1, 1, 2, 128, None, None, None, None, None, 0, None, None)
+    assert rc == 0
+
+
+def test_partials_and_workspace_sizes(lib):
+    p = lib.mesh_attn_plan_create(16384, 16, True)
+    assert lib.mesh_attn_partials_size(p, 1, 16, 128) == (16 * 58 * 1024 * 128, 16 * 58 * 1024)
+    assert lib.mesh_attn_workspace_size(p) >= 17 * 4 + 58 * 16 + 136 * 4

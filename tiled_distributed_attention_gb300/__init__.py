@@ -1,0 +1,277 @@
+"""Python binding of libmesh_attn.so, the single-GPU Mesh-Attention hot path for sm_103a.
+
+Argument marshalling only: every step of the computation (tile map, greedy order, tile
+attention, LSE merge) runs in the C++ planner and the CUDA kernels behind the C ABI declared
+in include/mesh_attn.h.  The functions carry the same names as the C entry points.  PyTorch
+supplies device memory and streams; nothing here computes attention, and there is no CPU
+fallback: if the library is missing, load_library() raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmesh_attn.so")
+
+MESH_ATTN_OK = 0
+MESH_ATTN_F32 = 0
+MESH_ATTN_BF16 = 1
+MESH_ATTN_STATUS_WORDS = 4
+STATUS_NAMES = {
+    0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED", 3: "ERR_MISALIGNED", 4: "ERR_CUDA",
+    5: "ERR_DEVICE_TIMEOUT", 6: "ERR_OUT_OF_RANGE", 7: "ERR_INTERNAL", 8: "ERR_NO_MEMORY",
+    9: "ERR_WORKSPACE",
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+c_i32, c_i64, c_sz, c_f32, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float, ctypes.c_void_p
+P_i32 = ctypes.POINTER(c_i32)
+P_i64 = ctypes.POINTER(c_i64)
+P_sz = ctypes.POINTER(c_sz)
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("S", c_i64), ("L", c_i64), ("P", c_i32), ("R", c_i32), ("causal", c_i32), ("kvr", c_i32),
+                ("greedy", c_i32), ("n_slots", c_i32), ("n_steps", c_i32), ("reserved", c_i32),
+                ("n_kv_entries", c_i64), ("n_live_blocks", c_i64)]
+
+
+_SIGS = {
+    "mesh_attn_plan_create": (c_i32, [c_i64, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_vp)]),
+    "mesh_attn_plan_destroy": (c_i32, [c_vp]),
+    "mesh_attn_plan_get_info": (c_i32, [c_vp, ctypes.POINTER(PlanInfo)]),
+    "mesh_attn_plan_tiles": (c_i32, [c_vp, P_i32, P_i32]),
+    "mesh_attn_plan_slots": (c_i32, [c_vp, P_i32]),
+    "mesh_attn_plan_order": (c_i32, [c_vp, P_i32, P_i32, P_i32, P_i32]),
+    "mesh_attn_plan_volumes": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, P_i32, P_i64, P_i64]),
+    "mesh_attn_partials_size": (c_i32, [c_vp, c_i32, c_i32, c_i32, P_sz, P_sz]),
+    "mesh_attn_workspace_size": (c_i32, [c_vp, P_sz]),
+    "mesh_attn_tile_fwd": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_f32, c_vp, c_vp,
+                                   c_vp, c_sz, c_vp, c_vp]),
+    "mesh_attn_merge": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    "mesh_attn_read_status": (c_i32, [c_vp, c_vp, P_i32]),
+    "mesh_attn_status_string": (ctypes.c_char_p, [c_i32]),
+    "mesh_attn_last_error": (ctypes.c_char_p, []),
+    "mesh_attn_set_wait_limit_ns": (c_i32, [c_i64]),
+}
+
+
+class MeshAttnError(RuntimeError):
+    def __init__(self, code: int, where: str, msg: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmesh_attn.so (built by __graft_entry__.build()) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(code: int, where: str):
+    if code != MESH_ATTN_OK:
+        msg = _lib.mesh_attn_last_error().decode()
+        raise MeshAttnError(code, where, msg)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return MESH_ATTN_BF16
+    if dt == torch.float32:
+        return MESH_ATTN_F32
+    raise TypeError(f"unsupported dtype {dt}: use torch.bfloat16 or torch.float32")
+
+
+class Plan:
+    """Owning handle of a mesh_attn_plan (host memory, immutable)."""
+
+    def __init__(self, handle: ctypes.c_void_p):
+        self._h = handle
+        info = PlanInfo()
+        _check(_lib.mesh_attn_plan_get_info(self._h, ctypes.byref(info)), "mesh_attn_plan_get_info")
+        self.info = info
+
+    @property
+    def handle(self):
+        return self._h
+
+    def __getattr__(self, name):
+        if name in ("S", "L", "P", "R", "causal", "kvr", "greedy", "n_slots", "n_steps", "n_kv_entries",
+                    "n_live_blocks"):
+            return getattr(self.__dict__["info"], name)
+        raise AttributeError(name)
+
+    def close(self):
+        if self._h is not None and _lib is not None:
+            _lib.mesh_attn_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _i32(n: int):
+    return (c_i32 * max(n, 1))()
+
+
+def mesh_attn_plan_create(S: int, P: int, causal: bool, kvr: bool = True, greedy: bool = True) -> Plan:
+    load_library()
+    h = c_vp()
+    _check(_lib.mesh_attn_plan_create(S, P, int(causal), int(kvr), int(greedy), ctypes.byref(h)),
+           "mesh_attn_plan_create")
+    return Plan(h)
+
+
+def mesh_attn_plan_tiles(plan: Plan):
+    n = plan.P * plan.R
+    q, kv = _i32(n), _i32(n)
+    _check(_lib.mesh_attn_plan_tiles(plan.handle, q, kv), "mesh_attn_plan_tiles")
+    R = plan.R
+    return ([list(q[t * R:(t + 1) * R]) for t in range(plan.P)], [list(kv[t * R:(t + 1) * R]) for t in range(plan.P)])
+
+
+def mesh_attn_plan_slots(plan: Plan):
+    off = _i32(plan.P + 1)
+    _check(_lib.mesh_attn_plan_slots(plan.handle, off), "mesh_attn_plan_slots")
+    return list(off[:plan.P + 1])
+
+
+def mesh_attn_plan_order(plan: Plan):
+    n = plan.n_slots
+    items, steps, kv_off, kv_list = _i32(3 * n), _i32(n), _i32(n + 1), _i32(plan.n_kv_entries)
+    _check(_lib.mesh_attn_plan_order(plan.handle, items, steps, kv_off, kv_list), "mesh_attn_plan_order")
+    off = list(kv_off[:n + 1])
+    kvl = list(kv_list[:plan.n_kv_entries])
+    return ([tuple(items[3 * i:3 * i + 3]) for i in range(n)], list(steps[:n]),
+            [kvl[off[i]:off[i + 1]] for i in range(n)])
+
+
+def mesh_attn_plan_volumes(plan: Plan, Hq: int, Hkv: int, d: int, dtype: torch.dtype = torch.bfloat16):
+    counts = _i32(3 * plan.P)
+    byts = (c_i64 * (3 * plan.P))()
+    ring = c_i64()
+    _check(_lib.mesh_attn_plan_volumes(plan.handle, Hq, Hkv, d, _dtype_code(dtype), counts, byts, ctypes.byref(ring)),
+           "mesh_attn_plan_volumes")
+    P = plan.P
+    return ([tuple(counts[3 * v:3 * v + 3]) for v in range(P)], [tuple(byts[3 * v:3 * v + 3]) for v in range(P)],
+            ring.value)
+
+
+def mesh_attn_partials_size(plan: Plan, B: int, Hq: int, d: int) -> Tuple[int, int]:
+    o, l = c_sz(), c_sz()
+    _check(_lib.mesh_attn_partials_size(plan.handle, B, Hq, d, ctypes.byref(o), ctypes.byref(l)),
+           "mesh_attn_partials_size")
+    return o.value, l.value
+
+
+def mesh_attn_workspace_size(plan: Plan) -> int:
+    n = c_sz()
+    _check(_lib.mesh_attn_workspace_size(plan.handle, ctypes.byref(n)), "mesh_attn_workspace_size")
+    return n.value
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed device status block (MESH_ATTN_STATUS_WORDS int32)."""
+    return torch.zeros(MESH_ATTN_STATUS_WORDS, dtype=torch.int32, device=device or "cuda")
+
+
+def new_workspace(plan: Plan, device=None) -> torch.Tensor:
+    return torch.empty(max(mesh_attn_workspace_size(plan), 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def new_partials(plan: Plan, B: int, Hq: int, d: int, device=None):
+    no, nl = mesh_attn_partials_size(plan, B, Hq, d)
+    dev = device or "cuda"
+    return (torch.empty(max(no, 4), dtype=torch.float32, device=dev),
+            torch.empty(max(nl, 4), dtype=torch.float32, device=dev))
+
+
+def mesh_attn_tile_fwd(plan: Plan, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float],
+                       partial_o: torch.Tensor, partial_lse: torch.Tensor, workspace: torch.Tensor,
+                       status: torch.Tensor, stream=None) -> None:
+    B, Hq, S, d = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
+    _check(_lib.mesh_attn_tile_fwd(plan.handle, _dtype_code(q.dtype), B, Hq, Hkv, d, _ptr(q), _ptr(k), _ptr(v),
+                                   float(scale), _ptr(partial_o), _ptr(partial_lse), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _ptr(status),
+                                   _stream_handle(stream)), "mesh_attn_tile_fwd")
+
+
+def mesh_attn_merge(plan: Plan, B: int, Hq: int, d: int, partial_o: torch.Tensor, partial_lse: torch.Tensor,
+                    O: torch.Tensor, LSE: torch.Tensor, workspace: torch.Tensor, status: torch.Tensor,
+                    stream=None) -> None:
+    _check(_lib.mesh_attn_merge(plan.handle, _dtype_code(O.dtype), B, Hq, d, _ptr(partial_o), _ptr(partial_lse),
+                                _ptr(O), _ptr(LSE), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _ptr(status), _stream_handle(stream)), "mesh_attn_merge")
+
+
+def mesh_attn_read_status(status: torch.Tensor, stream=None) -> int:
+    out = c_i32()
+    _check(_lib.mesh_attn_read_status(_ptr(status), _stream_handle(stream), ctypes.byref(out)),
+           "mesh_attn_read_status")
+    return out.value
+
+
+def mesh_attn_set_wait_limit_ns(ns: int) -> None:
+    load_library()
+    _check(_lib.mesh_attn_set_wait_limit_ns(int(ns)), "mesh_attn_set_wait_limit_ns")
+
+
+def mesh_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, causal: bool, kvr: bool = True,
+                   greedy: bool = True, scale: Optional[float] = None, plan: Optional[Plan] = None,
+                   return_partials: bool = False, check_status: bool = True):
+    """Whole hot path on the current stream: plan, tile forward, LSE merge.
+
+    q [B,Hq,S,d], k/v [B,Hkv,S,d] CUDA tensors (bf16 or fp32).  Returns (O, LSE) with O in
+    q's dtype and LSE fp32; with return_partials also (partial_o, partial_lse).
+    """
+    B, Hq, S, d = q.shape
+    plan = plan or mesh_attn_plan_create(S, P, causal, kvr, greedy)
+    po, pl = new_partials(plan, B, Hq, d, q.device)
+    ws = new_workspace(plan, q.device)
+    st = new_status(q.device)
+    O = torch.empty_like(q)
+    LSE = torch.empty(B, Hq, S, dtype=torch.float32, device=q.device)
+    mesh_attn_tile_fwd(plan, q, k, v, scale, po, pl, ws, st)
+    mesh_attn_merge(plan, B, Hq, d, po, pl, O, LSE, ws, st)
+    if check_status:
+        code = mesh_attn_read_status(st)
+        if code != 0:
+            raise MeshAttnError(code, "device", f"status block {st.tolist()}")
+    if return_partials:
+        return O, LSE, po, pl
+    return O, LSE

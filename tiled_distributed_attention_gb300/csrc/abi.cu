@@ -1,0 +1,328 @@
+// extern "C" entry points declared in mesh_attn.h: argument validation, plan access, work-list
+// upload into the caller's workspace and kernel dispatch.  No exception crosses this layer and
+// nothing is enqueued before every host-side check has passed.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <stdexcept>
+#include <string>
+
+#include "internal.h"
+
+struct mesh_attn_plan {
+  mesh::Plan p;
+};
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<int64_t> g_wait_limit_ns{2000000000LL};
+
+int fail(int code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what, const std::string& extra = std::string()) {
+  g_err = std::string(what) + ": " + cudaGetErrorString(e) + (extra.empty() ? "" : " (" + extra + ")");
+  return MESH_ATTN_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+template <typename F>
+int guarded(F&& f) {
+  try {
+    g_err.clear();
+    return f();
+  } catch (const std::bad_alloc&) {
+    return fail(MESH_ATTN_ERR_NO_MEMORY, "host allocation failed");
+  } catch (const std::invalid_argument& e) {
+    return fail(MESH_ATTN_ERR_INVALID_ARG, e.what());
+  } catch (const std::exception& e) {
+    return fail(MESH_ATTN_ERR_INTERNAL, e.what());
+  } catch (...) {
+    return fail(MESH_ATTN_ERR_INTERNAL, "unknown exception");
+  }
+}
+
+int check_common(const mesh_attn_plan* plan, int32_t B, int32_t Hq, int32_t d) {
+  if (!plan) return fail(MESH_ATTN_ERR_INVALID_ARG, "plan is NULL");
+  if (B < 0 || Hq < 0) return fail(MESH_ATTN_ERR_INVALID_ARG, "B and Hq must be >= 0");
+  if (d != 64 && d != 128) return fail(MESH_ATTN_ERR_UNSUPPORTED, "d must be 64 or 128");
+  const mesh::Plan& pl = plan->p;
+  // rows are addressed with 32-bit TMA coordinates and 32-bit grid indices
+  if ((int64_t)B * Hq * pl.S >= (int64_t)1 << 31)
+    return fail(MESH_ATTN_ERR_UNSUPPORTED, "B * Hq * S must be < 2^31");
+  return MESH_ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mesh_attn_plan_create(int64_t S, int32_t P, int32_t causal, int32_t kvr, int32_t greedy,
+                          mesh_attn_plan** out) {
+  return guarded([&] {
+    if (!out) return fail(MESH_ATTN_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    for (int32_t f : {causal, kvr, greedy})
+      if (f != 0 && f != 1) return fail(MESH_ATTN_ERR_INVALID_ARG, "causal, kvr and greedy must be 0 or 1");
+    mesh_attn_plan* p = new mesh_attn_plan();
+    try {
+      mesh::build_plan(p->p, S, P, causal != 0, kvr != 0, greedy != 0);
+    } catch (...) {
+      delete p;
+      throw;
+    }
+    *out = p;
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_plan_destroy(mesh_attn_plan* plan) {
+  delete plan;
+  return MESH_ATTN_OK;
+}
+
+int mesh_attn_plan_get_info(const mesh_attn_plan* plan, mesh_attn_plan_info* out) {
+  return guarded([&] {
+    if (!plan || !out) return fail(MESH_ATTN_ERR_INVALID_ARG, "plan or out is NULL");
+    const mesh::Plan& p = plan->p;
+    std::memset(out, 0, sizeof(*out));
+    out->S = p.S;
+    out->L = p.L;
+    out->P = p.P;
+    out->R = p.R;
+    out->causal = p.causal;
+    out->kvr = p.kvr;
+    out->greedy = p.greedy;
+    out->n_slots = p.n_slots();
+    out->n_steps = p.n_steps;
+    out->n_kv_entries = (int64_t)p.kv_list.size();
+    out->n_live_blocks = p.n_live;
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_plan_tiles(const mesh_attn_plan* plan, int32_t* q_parts, int32_t* kv_parts) {
+  return guarded([&] {
+    if (!plan || !q_parts || !kv_parts) return fail(MESH_ATTN_ERR_INVALID_ARG, "NULL argument");
+    std::memcpy(q_parts, plan->p.q_parts.data(), plan->p.q_parts.size() * sizeof(int32_t));
+    std::memcpy(kv_parts, plan->p.kv_parts.data(), plan->p.kv_parts.size() * sizeof(int32_t));
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_plan_slots(const mesh_attn_plan* plan, int32_t* slot_off) {
+  return guarded([&] {
+    if (!plan || !slot_off) return fail(MESH_ATTN_ERR_INVALID_ARG, "NULL argument");
+    std::memcpy(slot_off, plan->p.slot_off.data(), plan->p.slot_off.size() * sizeof(int32_t));
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_plan_order(const mesh_attn_plan* plan, int32_t* items, int32_t* item_step, int32_t* kv_off,
+                         int32_t* kv_list) {
+  return guarded([&] {
+    if (!plan) return fail(MESH_ATTN_ERR_INVALID_ARG, "plan is NULL");
+    const mesh::Plan& p = plan->p;
+    if (items) std::memcpy(items, p.items.data(), p.items.size() * sizeof(int32_t));
+    if (item_step) std::memcpy(item_step, p.item_step.data(), p.item_step.size() * sizeof(int32_t));
+    if (kv_off) std::memcpy(kv_off, p.kv_off.data(), p.kv_off.size() * sizeof(int32_t));
+    if (kv_list) std::memcpy(kv_list, p.kv_list.data(), p.kv_list.size() * sizeof(int32_t));
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_plan_volumes(const mesh_attn_plan* plan, int32_t Hq, int32_t Hkv, int32_t d, mesh_attn_dtype dtype,
+                           int32_t* counts, int64_t* bytes, int64_t* ring_bytes) {
+  return guarded([&] {
+    if (!plan) return fail(MESH_ATTN_ERR_INVALID_ARG, "plan is NULL");
+    if (Hq < 0 || Hkv < 0 || d < 0) return fail(MESH_ATTN_ERR_INVALID_ARG, "Hq, Hkv and d must be >= 0");
+    if (dtype != MESH_ATTN_F32 && dtype != MESH_ATTN_BF16) return fail(MESH_ATTN_ERR_INVALID_ARG, "bad dtype");
+    const mesh::Plan& p = plan->p;
+    const int64_t es = dtype == MESH_ATTN_BF16 ? 2 : 4;
+    const int64_t qb = p.L * Hq * d * es;
+    const int64_t kvb = 2 * p.L * Hkv * d * es;
+    const int64_t ob = p.L * Hq * (4 * (int64_t)d + 4);
+    for (int32_t v = 0; v < p.P; ++v) {
+      const int32_t* c = &p.recv[(size_t)v * 3];
+      if (counts) {
+        counts[3 * v + 0] = c[0];
+        counts[3 * v + 1] = c[1];
+        counts[3 * v + 2] = c[2];
+      }
+      if (bytes) {
+        bytes[3 * v + 0] = c[0] * qb;
+        bytes[3 * v + 1] = c[1] * kvb;
+        bytes[3 * v + 2] = c[2] * ob;
+      }
+    }
+    if (ring_bytes) *ring_bytes = (int64_t)(p.P - 1) * kvb;
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_partials_size(const mesh_attn_plan* plan, int32_t B, int32_t Hq, int32_t d, size_t* o_elems,
+                            size_t* lse_elems) {
+  return guarded([&] {
+    if (!plan || !o_elems || !lse_elems) return fail(MESH_ATTN_ERR_INVALID_ARG, "NULL argument");
+    if (B < 0 || Hq < 0 || d < 0) return fail(MESH_ATTN_ERR_INVALID_ARG, "B, Hq and d must be >= 0");
+    const size_t rows = (size_t)B * Hq * plan->p.n_slots() * (size_t)plan->p.L;
+    *lse_elems = rows;
+    *o_elems = rows * (size_t)d;
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_workspace_size(const mesh_attn_plan* plan, size_t* bytes) {
+  return guarded([&] {
+    if (!plan || !bytes) return fail(MESH_ATTN_ERR_INVALID_ARG, "NULL argument");
+    *bytes = mesh::workspace_layout(plan->p).total;
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_tile_fwd(const mesh_attn_plan* plan, mesh_attn_dtype in_dtype, int32_t B, int32_t Hq, int32_t Hkv,
+                       int32_t d, const void* Q, const void* K, const void* V, float scale, float* partial_o,
+                       float* partial_lse, void* workspace, size_t workspace_bytes, int32_t* d_status,
+                       void* stream) {
+  return guarded([&] {
+    int rc = check_common(plan, B, Hq, d);
+    if (rc) return rc;
+    if (in_dtype != MESH_ATTN_F32 && in_dtype != MESH_ATTN_BF16)
+      return fail(MESH_ATTN_ERR_INVALID_ARG, "in_dtype must be MESH_ATTN_F32 or MESH_ATTN_BF16");
+    if (Hkv < 1 || Hq % Hkv != 0) return fail(MESH_ATTN_ERR_INVALID_ARG, "need Hkv >= 1 and Hq % Hkv == 0");
+    if (!(scale > 0.f) || !std::isfinite(scale)) return fail(MESH_ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+    const mesh::Plan& pl = plan->p;
+    if (pl.n_slots() == 0 || B == 0 || Hq == 0) return (int)MESH_ATTN_OK;
+    if (!Q || !K || !V || !partial_o || !partial_lse || !workspace || !d_status)
+      return fail(MESH_ATTN_ERR_INVALID_ARG, "a tensor, workspace or status pointer is NULL");
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(partial_o, 16) ||
+        !aligned(partial_lse, 4) || !aligned(workspace, 16) || !aligned(d_status, 4))
+      return fail(MESH_ATTN_ERR_MISALIGNED, "Q, K, V, partial_o and workspace must be 16-byte aligned");
+    const mesh::WorkspaceLayout wl = mesh::workspace_layout(pl);
+    if (workspace_bytes < wl.total)
+      return fail(MESH_ATTN_ERR_WORKSPACE, "workspace needs " + std::to_string(wl.total) + " bytes");
+    char* ws = static_cast<char*>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(ws + wl.items_off, pl.dev_items.data(), wl.items_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "work-list upload");
+    e = cudaMemcpyAsync(ws + wl.kv_off, pl.kv_list.data(), wl.kv_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "KV-list upload");
+    mesh::TileArgs a{};
+    a.Q = Q;
+    a.K = K;
+    a.V = V;
+    a.part_o = partial_o;
+    a.part_lse = partial_lse;
+    a.items = reinterpret_cast<const mesh::DevItem*>(ws + wl.items_off);
+    a.kv_list = reinterpret_cast<const int32_t*>(ws + wl.kv_off);
+    a.counter = reinterpret_cast<uint32_t*>(ws + wl.counter_off);
+    a.status = d_status;
+    a.S = pl.S;
+    a.L = pl.L;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.P = pl.P;
+    a.n_items = pl.n_slots();
+    a.n_slots = pl.n_slots();
+    a.causal = pl.causal ? 1 : 0;
+    a.scale = scale;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    a.wait_limit_ns = g_wait_limit_ns.load();
+    std::string err;
+    const int ce = (in_dtype == MESH_ATTN_BF16) ? mesh::launch_tile_fwd_tc(a, stream, &err)
+                                                : mesh::launch_tile_fwd_simt(a, MESH_ATTN_F32, stream, &err);
+    if (ce != (int)cudaSuccess) return fail(MESH_ATTN_ERR_CUDA, err.empty() ? cudaGetErrorString((cudaError_t)ce) : err);
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_merge(const mesh_attn_plan* plan, mesh_attn_dtype out_dtype, int32_t B, int32_t Hq, int32_t d,
+                    const float* partial_o, const float* partial_lse, void* O, float* LSE, void* workspace,
+                    size_t workspace_bytes, int32_t* d_status, void* stream) {
+  return guarded([&] {
+    int rc = check_common(plan, B, Hq, d);
+    if (rc) return rc;
+    if (out_dtype != MESH_ATTN_F32 && out_dtype != MESH_ATTN_BF16)
+      return fail(MESH_ATTN_ERR_INVALID_ARG, "out_dtype must be MESH_ATTN_F32 or MESH_ATTN_BF16");
+    const mesh::Plan& pl = plan->p;
+    if (pl.S == 0 || B == 0 || Hq == 0) return (int)MESH_ATTN_OK;
+    if (!partial_o || !partial_lse || !O || !LSE || !workspace || !d_status)
+      return fail(MESH_ATTN_ERR_INVALID_ARG, "a tensor, workspace or status pointer is NULL");
+    if (!aligned(partial_o, 16) || !aligned(partial_lse, 4) || !aligned(O, 16) || !aligned(LSE, 4) ||
+        !aligned(workspace, 16) || !aligned(d_status, 4))
+      return fail(MESH_ATTN_ERR_MISALIGNED, "partial_o, O and workspace must be 16-byte aligned");
+    const mesh::WorkspaceLayout wl = mesh::workspace_layout(pl);
+    if (workspace_bytes < wl.total)
+      return fail(MESH_ATTN_ERR_WORKSPACE, "workspace needs " + std::to_string(wl.total) + " bytes");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(workspace, pl.slot_off.data(), wl.slot_off_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "slot-offset upload");
+    mesh::MergeArgs a{};
+    a.part_o = partial_o;
+    a.part_lse = partial_lse;
+    a.slot_off = static_cast<const int32_t*>(workspace);
+    a.O = O;
+    a.LSE = LSE;
+    a.status = d_status;
+    a.S = pl.S;
+    a.L = pl.L;
+    a.B = B;
+    a.Hq = Hq;
+    a.d = d;
+    a.P = pl.P;
+    a.n_slots = pl.n_slots();
+    std::string err;
+    const int ce = mesh::launch_merge(a, out_dtype, stream, &err);
+    if (ce != (int)cudaSuccess) return fail(MESH_ATTN_ERR_CUDA, err.empty() ? cudaGetErrorString((cudaError_t)ce) : err);
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_read_status(const int32_t* d_status, void* stream, int32_t* out) {
+  return guarded([&] {
+    if (!d_status || !out) return fail(MESH_ATTN_ERR_INVALID_ARG, "NULL argument");
+    int32_t h = 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&h, d_status, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e, "status copy");
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
+    *out = h;
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+const char* mesh_attn_status_string(int status) {
+  switch (status) {
+    case MESH_ATTN_OK: return "ok";
+    case MESH_ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case MESH_ATTN_ERR_UNSUPPORTED: return "unsupported";
+    case MESH_ATTN_ERR_MISALIGNED: return "misaligned pointer";
+    case MESH_ATTN_ERR_CUDA: return "CUDA error";
+    case MESH_ATTN_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case MESH_ATTN_ERR_OUT_OF_RANGE: return "device index out of range";
+    case MESH_ATTN_ERR_INTERNAL: return "internal error";
+    case MESH_ATTN_ERR_NO_MEMORY: return "host out of memory";
+    case MESH_ATTN_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+const char* mesh_attn_last_error(void) { return g_err.c_str(); }
+
+int mesh_attn_set_wait_limit_ns(int64_t ns) {
+  if (ns < 0) return fail(MESH_ATTN_ERR_INVALID_ARG, "ns must be >= 0");
+  g_wait_limit_ns.store(ns);
+  return MESH_ATTN_OK;
+}
+
+}  // extern "C"
