@@ -1,0 +1,325 @@
+"""Benchmark of the Mesh-Attention hot path on GB300: one step = tile forward over every
+(Q partition, tile) item of the plan + LSE merge, on a synthetic workload resident in HBM.
+
+Prints one JSON line (rank 0).  Default workload: bf16 causal, B=1, Hq=Hkv=16, S=16384,
+d=128, P=16 partitions of 1024 tokens on a 4x4 mesh with KV Partition Rotation and greedy
+order.  `--impl reference` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mesh_inputs import WORKLOADS, make_qkv, sample_rows  # noqa: E402
+
+METRIC = "mesh-tiled attention fwd TFLOP/s & % bf16 tensor peak; merge HBM GB/s (1 GB300)"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def algorithmic_flops(w) -> float:
+    """4 d per visible (query, key) pair: QK^T and PV, 2 flops per multiply-add each."""
+    pairs = w.S * (w.S + 1) // 2 if w.causal else w.S * w.S
+    return 4.0 * w.d * w.B * w.Hq * pairs
+
+
+def sample_flops(w, rows: np.ndarray) -> float:
+    vis = (rows + 1).sum() if w.causal else rows.size * w.S
+    return 4.0 * w.d * float(vis)
+
+
+def merge_bytes(w, n_slots: int) -> float:
+    es = 2 if w.dtype == "bf16" else 4
+    read = n_slots * w.L * w.Hq * w.B * (4 * w.d + 4)
+    write = w.B * w.Hq * w.S * (es * w.d + 4)
+    return float(read + write)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+_INPUTS = {}
+
+
+def time_oracle(w, n_rows: int, heads, threads: int):
+    """fp64 oracle on n_rows seeded rows of the given heads; returns (seconds, algorithmic flops)."""
+    from oracle.attention import attention_rows, default_scale
+    torch.set_num_threads(threads)
+    if (w.name, n_rows) not in _INPUTS:
+        _INPUTS[(w.name, n_rows)] = (make_qkv(w), sample_rows(w, n_rows))
+    (q, k, v), rows = _INPUTS[(w.name, n_rows)]
+    g = w.Hq // w.Hkv
+    t0 = time.perf_counter()
+    fl = 0.0
+    for h in heads:
+        pos = torch.as_tensor(rows[0, h])
+        attention_rows(q[0, h].double()[pos], pos, k[0, h // g], v[0, h // g], default_scale(w.d), w.causal)
+        fl += sample_flops(w, rows[0, h])
+    return time.perf_counter() - t0, fl
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    rows_per_step = 256
+    for i in range(args.warmup):
+        time_oracle(w, rows_per_step, [i % w.Hq], threads)
+    secs, fl = 0.0, 0.0
+    for i in range(args.steps):
+        s, f = time_oracle(w, rows_per_step, [i % w.Hq], threads)
+        secs += s
+        fl += f
+    value = fl / secs / 1e12
+    sample = f"{rows_per_step} seeded query rows of one head per step (head cycles), fp64 oracle, full key range"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d, "in_dtype": w.dtype,
+            "causal": w.causal, "P": w.P, "mesh": f"{w.R}x{w.R}", "kvr": w.kvr, "greedy": w.greedy,
+            "k_scale": w.k_scale, "l2": "inputs and partials larger than L2 (no flush)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="bf16_causal_16k", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import tiled_distributed_attention_gb300 as m
+    m.load_library()
+    ws, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # cpu baseline first (before any GPU work is queued), rank 0 at N=1 only
+    cpu_base = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        secs, fl = time_oracle(w, 4096, range(w.Hq), threads)
+        cpu_base = {"value": fl / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+                    "sample": f"4096 seeded query rows x {w.Hq} heads of the workload, fp64, {secs:.1f} s"}
+
+    q, k, v = make_qkv(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    plan = m.mesh_attn_plan_create(w.S, w.P, w.causal, w.kvr, w.greedy)
+    po, pl = m.new_partials(plan, w.B, w.Hq, w.d, dev)
+    wsp = m.new_workspace(plan, dev)
+    st = m.new_status(dev)
+    O = torch.empty_like(qd)
+    LSE = torch.empty(w.B, w.Hq, w.S, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        m.mesh_attn_tile_fwd(plan, qd, kd, vd, None, po, pl, wsp, st, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        m.mesh_attn_merge(plan, w.B, w.Hq, w.d, po, pl, O, LSE, wsp, st, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    code = m.mesh_attn_read_status(st, stream)
+    if code != 0:
+        raise RuntimeError(f"device status {code} during warm-up: {st.tolist()}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    code = m.mesh_attn_read_status(st, stream)
+    if code != 0:
+        raise RuntimeError(f"device status {code} in the timed region: {st.tolist()}")
+    total_ms = t_start.elapsed_time(t_end)
+    tile_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    merge_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = t.item()
+    ms_per_step = total_ms / args.steps
+    flops = algorithmic_flops(w)
+    value = ws * flops / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public call, host buffers in pinned memory
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        Oh = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
+        Lh = torch.empty(LSE.shape, dtype=LSE.dtype, pin_memory=True)
+
+        def e2e_step():
+            a, b_, c = qh.to(dev, non_blocking=True), kh.to(dev, non_blocking=True), vh.to(dev, non_blocking=True)
+            Od, Ld = m.mesh_attention(a, b_, c, w.P, w.causal, w.kvr, w.greedy, check_status=False)
+            Oh.copy_(Od, non_blocking=True)
+            Lh.copy_(Ld, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 20))
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e_ms = e0.elapsed_time(e1) / n_e2e
+        if ws > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = t.item()
+        es = q.element_size()
+        e2e = {"value": ws * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": int((q.numel() + k.numel() + v.numel()) * es),
+               "d2h_bytes_per_step": int(O.numel() * O.element_size() + LSE.numel() * 4),
+               "ms_per_step": e_ms, "steps": n_e2e}
+
+    if rank != 0:
+        return
+    peaks, peak_kind = load_peaks()
+    tile_tflops = flops / (tile_ms * 1e-3) / 1e12
+    mbytes = merge_bytes(w, plan.n_slots)
+    merge_gbs = mbytes / (merge_ms * 1e-3) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            tr = json.load(f)
+        traffic = tr.get(w.name, {}).get("tile_fwd")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": workload_config(w),
+        "roofline": {"bound": "tensor", "achieved": tile_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tile_tflops / peaks["bf16_tflops"], "traffic": traffic,
+                     "kernel": "tile_fwd_tc_kernel", "peak_kind": f"{peak_kind} bf16 dense burst"},
+        "merge": {"bound": "hbm", "achieved": merge_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                  "frac": merge_gbs / peaks["hbm_gbs"], "bytes_per_launch": mbytes, "ms": merge_ms},
+        "tile_fwd_ms": tile_ms, "merge_ms": merge_ms,
+        "cpu_baseline": cpu_base, "e2e": e2e, "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
