@@ -1,0 +1,59 @@
+"""Device-side failure reporting without a GPU fault.
+
+The wait limit is set to 0 so every device wait that is not already satisfied gives up at
+once: the tile kernel must record MESH_ATTN_ERR_DEVICE_TIMEOUT in the status block, drain its
+copies, free its tensor memory and return.  Later kernels see the non-zero status and skip
+their work.  After clearing the status and restoring the limit, the same context computes
+correct results again.
+"""
+import pytest
+import torch
+
+from mesh_inputs import Workload, make_qkv
+from tests.gpu_helpers import check_full
+
+pytestmark = pytest.mark.gpu
+
+
+def test_wait_timeout_reports_status_and_context_survives(lib):
+    w = Workload(120, "status", 1, 2, 1, 2048, 128, "bf16", True, 4)
+    q, k, v = make_qkv(w)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    plan = lib.mesh_attn_plan_create(w.S, w.P, w.causal, True, True)
+    po, pl = lib.new_partials(plan, 1, 2, 128)
+    ws = lib.new_workspace(plan)
+    st = lib.new_status()
+    O = torch.full_like(qd, 7.0)
+    LSE = torch.full((1, 2, w.S), 7.0, device="cuda")
+    lib.mesh_attn_set_wait_limit_ns(0)
+    try:
+        lib.mesh_attn_tile_fwd(plan, qd, kd, vd, None, po, pl, ws, st)
+        code = lib.mesh_attn_read_status(st)
+    finally:
+        lib.mesh_attn_set_wait_limit_ns(2_000_000_000)
+    assert code == 5, f"status block {st.tolist()}"
+    assert st[1].item() in (1, 2, 3)  # softmax, MMA or load role gave up
+    # a set status makes later kernels skip their work
+    lib.mesh_attn_merge(plan, 1, 2, 128, po, pl, O, LSE, ws, st)
+    assert lib.mesh_attn_read_status(st) == 5
+    assert bool((O == 7.0).all()) and bool((LSE == 7.0).all())
+    # the context is still usable
+    st.zero_()
+    lib.mesh_attn_tile_fwd(plan, qd, kd, vd, None, po, pl, ws, st)
+    lib.mesh_attn_merge(plan, 1, 2, 128, po, pl, O, LSE, ws, st)
+    assert lib.mesh_attn_read_status(st) == 0
+    check_full(w, O, LSE, q, k, v)
+
+
+def test_empty_and_degenerate_launches(lib):
+    """B = 0, Hq = 0 and an empty sequence enqueue nothing and leave outputs untouched."""
+    plan = lib.mesh_attn_plan_create(0, 4, True)
+    st = lib.new_status()
+    O = torch.full((1, 2, 0, 128), 3.0, dtype=torch.bfloat16, device="cuda")
+    LSE = torch.empty((1, 2, 0), device="cuda")
+    ws = lib.new_workspace(plan)
+    po, pl = lib.new_partials(plan, 1, 2, 128)
+    q = torch.zeros((1, 2, 0, 128), dtype=torch.bfloat16, device="cuda")
+    lib.mesh_attn_tile_fwd(plan, q, q[:, :1], q[:, :1], None, po, pl, ws, st)
+    lib.mesh_attn_merge(plan, 1, 2, 128, po, pl, O, LSE, ws, st)
+    assert lib.mesh_attn_read_status(st) == 0
