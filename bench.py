@@ -301,9 +301,15 @@ def main():
     traffic = None
     prof = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(prof):
+        import hashlib
         with open(prof) as f:
-            tr = json.load(f)
-        traffic = tr.get(w.name, {}).get("tile_fwd")
+            rec = json.load(f).get(w.name, {}).get("tile_fwd")
+        src = os.path.join(ROOT, "tiled_distributed_attention_gb300", "csrc", "tile_fwd_tc.cu")
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        # counters only describe the kernel they were taken on
+        if rec and sha.startswith(rec["source_sha256_prefix"]):
+            traffic = rec["bytes"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
