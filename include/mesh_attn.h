@@ -158,6 +158,31 @@ int mesh_attn_tile_fwd(const mesh_attn_plan* plan, mesh_attn_dtype in_dtype, int
                        void* workspace, size_t workspace_bytes, int32_t* d_status,
                        void* stream);
 
+/* Maximum scratch of mesh_attn_tile_fwd_noalloc: device bytes every GPU that loads the
+ * library reserves for it until the process exits. */
+#define MESH_ATTN_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* Tile attention forward for callers that cannot allocate device memory.  The paper has no
+ * counterpart: this is a service of this library.
+ * Who needs it: code that runs where it may not call cudaMalloc -- under a framework whose
+ * caching allocator already owns the device memory pool (a direct allocation would fail or
+ * escape its accounting), inside an allocator or memory-pressure callback, or with a fixed,
+ * pre-reserved memory budget -- and so cannot provide the workspace mesh_attn_tile_fwd asks
+ * for.  It computes exactly what mesh_attn_tile_fwd computes, with the same arguments minus
+ * the workspace; the caller still passes the inputs, the partial outputs and d_status.
+ * The plan's work list goes into one fixed array of MESH_ATTN_NOALLOC_SCRATCH_BYTES inside the
+ * library instead.  A plan whose work list needs more (about 2.6 MB for P = 1024 causal; P =
+ * 4096 is too large) returns MESH_ATTN_ERR_WORKSPACE with the size in mesh_attn_last_error().
+ * The first call on a device looks up that device's array address (cudaGetSymbolAddress with
+ * the device current); make that first call before any stream capture.  No cudaMalloc, cudaFree
+ * or other allocating call is made.  All calls on a device share the one array and each call
+ * rewrites what the kernel reads from it, so calls that overlap on the GPU (other streams,
+ * other host threads) race: serialise them. */
+int mesh_attn_tile_fwd_noalloc(const mesh_attn_plan* plan, mesh_attn_dtype in_dtype, int32_t B,
+                               int32_t Hq, int32_t Hkv, int32_t d, const void* Q, const void* K,
+                               const void* V, float scale, float* partial_o, float* partial_lse,
+                               int32_t* d_status, void* stream);
+
 /* LSE merge (step 3): per (batch, head, row) over the slots of the row's partition,
  *   M = max_t lse_t, lse = M + ln sum_t exp(lse_t - M), O = sum_t exp(lse_t - lse) O_t;
  * a row whose slots are all -inf gets O = 0 and lse = -inf.

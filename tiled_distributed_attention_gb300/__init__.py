@@ -54,6 +54,8 @@ _SIGS = {
     "mesh_attn_workspace_size": (c_i32, [c_vp, P_sz]),
     "mesh_attn_tile_fwd": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_f32, c_vp, c_vp,
                                    c_vp, c_sz, c_vp, c_vp]),
+    "mesh_attn_tile_fwd_noalloc": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_f32, c_vp,
+                                           c_vp, c_vp, c_vp]),
     "mesh_attn_merge": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
     "mesh_attn_read_status": (c_i32, [c_vp, c_vp, P_i32]),
     "mesh_attn_status_string": (ctypes.c_char_p, [c_i32]),
@@ -229,6 +231,23 @@ def mesh_attn_tile_fwd(plan: Plan, q: torch.Tensor, k: torch.Tensor, v: torch.Te
                                    float(scale), _ptr(partial_o), _ptr(partial_lse), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _ptr(status),
                                    _stream_handle(stream)), "mesh_attn_tile_fwd")
+
+
+def mesh_attn_tile_fwd_noalloc(plan: Plan, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                               scale: Optional[float], partial_o: torch.Tensor, partial_lse: torch.Tensor,
+                               status: torch.Tensor, stream=None) -> None:
+    """mesh_attn_tile_fwd without a workspace: for callers that may not allocate device memory.
+    The work list goes into the library's fixed scratch array; calls overlapping on the GPU race."""
+    B, Hq, S, d = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
+    _check(_lib.mesh_attn_tile_fwd_noalloc(plan.handle, _dtype_code(q.dtype), B, Hq, Hkv, d, _ptr(q), _ptr(k),
+                                           _ptr(v), float(scale), _ptr(partial_o), _ptr(partial_lse), _ptr(status),
+                                           _stream_handle(stream)), "mesh_attn_tile_fwd_noalloc")
 
 
 def mesh_attn_merge(plan: Plan, B: int, Hq: int, d: int, partial_o: torch.Tensor, partial_lse: torch.Tensor,

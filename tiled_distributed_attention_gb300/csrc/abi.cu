@@ -12,10 +12,6 @@
 
 #include "internal.h"
 
-struct mesh_attn_plan {
-  mesh::Plan p;
-};
-
 namespace {
 
 thread_local std::string g_err;
@@ -61,6 +57,11 @@ int check_common(const mesh_attn_plan* plan, int32_t B, int32_t Hq, int32_t d) {
 }
 
 }  // namespace
+
+namespace mesh {
+int set_last_error(int code, const std::string& msg) { return fail(code, msg); }
+int64_t current_wait_limit_ns() { return g_wait_limit_ns.load(); }
+}  // namespace mesh
 
 extern "C" {
 

@@ -79,4 +79,14 @@ struct MergeArgs {
 };
 int launch_merge(const MergeArgs& a, mesh_attn_dtype out_dtype, void* stream, std::string* err);
 
+// Record `msg` as the calling thread's last error (mesh_attn_last_error) and return `code`.
+int set_last_error(int code, const std::string& msg);
+// Current process-wide bound on device-side waits (mesh_attn_set_wait_limit_ns).
+int64_t current_wait_limit_ns();
+
 }  // namespace mesh
+
+// The opaque handle of the C ABI.
+struct mesh_attn_plan {
+  mesh::Plan p;
+};
