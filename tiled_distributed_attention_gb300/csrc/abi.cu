@@ -215,6 +215,8 @@ int mesh_attn_tile_fwd(const mesh_attn_plan* plan, mesh_attn_dtype in_dtype, int
     if (e != cudaSuccess) return cuda_fail(e, "work-list upload");
     e = cudaMemcpyAsync(ws + wl.kv_off, pl.kv_list.data(), wl.kv_bytes, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_fail(e, "KV-list upload");
+    e = cudaMemsetAsync(ws + wl.counter_off, 0, 256, st);  // the kernel's unit counter starts at 0
+    if (e != cudaSuccess) return cuda_fail(e, "counter reset");
     mesh::TileArgs a{};
     a.Q = Q;
     a.K = K;

@@ -6,11 +6,14 @@
 // log-sum-exp rescaling of "环形注意力：突破长序列处理瓶颈的分布式计算范式",
 // §"数值稳定性：Log-Sum-Exp技术的分布式应用".
 //
-// A streaming HBM-bound kernel: one warp per output row.  Lane t first reads lse of slot t
-// (the slots of a row are L rows apart), the warp reduces max and sum with shuffles, then each
-// lane streams its d/32 contiguous columns of every slot's O_t row (16-byte loads for d = 128,
-// 512 contiguous bytes per slot per warp) and writes d/32 output values (8-byte bf16 or
-// 16-byte fp32 stores).
+// A streaming HBM-bound kernel.  One CTA of 256 threads owns ROWS consecutive rows of one
+// (batch, head, partition); because the slots of a partition hold the same rows at a stride of
+// L rows, the CTA's share of each slot is one contiguous block of ROWS * d floats (16 KB).
+//   1. the CTA reads its ROWS x n_slots LSE values (coalesced per slot) into shared memory;
+//   2. one warp turns them into per-row weights exp(lse_t - lse) and writes the row LSE;
+//   3. every thread streams 16-byte pieces of each slot's contiguous block (consecutive
+//      threads, consecutive addresses), scales them by the row weight and accumulates;
+//   4. the d/4 float4 sums per row are written as 8-byte bf16 (or 16-byte fp32) stores.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -23,113 +26,132 @@ namespace mesh {
 namespace merge {
 
 constexpr int THREADS = 256;
+constexpr int MAX_SLOTS = 64;  // R <= 64 for P <= 4096
 
-template <int E>
-struct Vec;
+template <typename OutT>
+__device__ __forceinline__ void store4(OutT* o, float4 v);
 template <>
-struct Vec<4> {
-  using T = float4;
-  static __device__ __forceinline__ void fma_into(float* acc, float w, const T& v) {
-    acc[0] = fmaf(w, v.x, acc[0]);
-    acc[1] = fmaf(w, v.y, acc[1]);
-    acc[2] = fmaf(w, v.z, acc[2]);
-    acc[3] = fmaf(w, v.w, acc[3]);
-  }
-};
-template <>
-struct Vec<2> {
-  using T = float2;
-  static __device__ __forceinline__ void fma_into(float* acc, float w, const T& v) {
-    acc[0] = fmaf(w, v.x, acc[0]);
-    acc[1] = fmaf(w, v.y, acc[1]);
-  }
-};
-
-template <int E>
-__device__ __forceinline__ void store_out(float* o, const float* acc) {
-  if constexpr (E == 4) *reinterpret_cast<float4*>(o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  else *reinterpret_cast<float2*>(o) = make_float2(acc[0], acc[1]);
+__device__ __forceinline__ void store4<float>(float* o, float4 v) {
+  *reinterpret_cast<float4*>(o) = v;
 }
-template <int E>
-__device__ __forceinline__ void store_out(__nv_bfloat16* o, const float* acc) {
-  const __nv_bfloat162 a = __floats2bfloat162_rn(acc[0], acc[1]);
-  if constexpr (E == 4) {
-    const __nv_bfloat162 c = __floats2bfloat162_rn(acc[2], acc[3]);
-    uint2 w;
-    w.x = *reinterpret_cast<const uint32_t*>(&a);
-    w.y = *reinterpret_cast<const uint32_t*>(&c);
-    *reinterpret_cast<uint2*>(o) = w;
-  } else {
-    *reinterpret_cast<__nv_bfloat162*>(o) = a;
-  }
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* o, float4 v) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 w;
+  w.x = *reinterpret_cast<const uint32_t*>(&a);
+  w.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(o) = w;
 }
 
 template <int D, typename OutT>
-__global__ void __launch_bounds__(THREADS) merge_kernel(const MergeArgs a) {
-  constexpr int E = D / 32;
-  using V = Vec<E>;
-  const int lane = threadIdx.x & 31;
-  const int64_t total = (int64_t)a.B * a.Hq * a.S;
-  const int64_t warps = ((int64_t)gridDim.x * THREADS) >> 5;
+__global__ void __launch_bounds__(THREADS) merge_kernel(const MergeArgs a, int n_rblk) {
+  constexpr int ROWS = 4096 / D;                // 16 KB of fp32 per slot per CTA
+  constexpr int V4_PER_ROW = D / 4;
+  constexpr int PER_THREAD = ROWS * V4_PER_ROW / THREADS;  // float4 outputs per thread (4)
+  __shared__ float w_s[MAX_SLOTS][ROWS];
   if (*reinterpret_cast<volatile int32_t*>(a.status) != 0) return;
-  for (int64_t w = ((int64_t)blockIdx.x * THREADS + threadIdx.x) >> 5; w < total; w += warps) {
-    const int64_t bh = w / a.S;
-    const int64_t i = w - bh * a.S;
-    const int p = (int)(i / a.L);
-    const int64_t r = i - (int64_t)p * a.L;
-    const int s0 = __ldg(a.slot_off + p);
-    const int ns = __ldg(a.slot_off + p + 1) - s0;
-    const int64_t base = (bh * a.n_slots + s0) * a.L + r;  // row of slot s0; slot t is t*L rows further
-    const float* lse_p = a.part_lse + base;
-    const typename V::T* o_p = reinterpret_cast<const typename V::T*>(a.part_o + base * D) + lane;
-    const int64_t o_stride = a.L * (D / E);  // in vectors, one slot
+  const int tid = threadIdx.x;
+  // CTA -> (bh, p, row block); 32-bit arithmetic: B*Hq*P*n_rblk < 2^31 is checked on the host
+  const int rb = (int)(blockIdx.x % (unsigned)n_rblk);
+  const int bhp = (int)(blockIdx.x / (unsigned)n_rblk);
+  const int p = bhp % a.P;
+  const int bh = bhp / a.P;
+  const int L = (int)a.L;
+  const int r0 = rb * ROWS;
+  const int nrows = min(ROWS, L - r0);
+  const int s0 = __ldg(a.slot_off + p);
+  const int ns = __ldg(a.slot_off + p + 1) - s0;
+  if (ns > MAX_SLOTS) {
+    if (tid == 0) record_error(a.status, MESH_ATTN_ERR_OUT_OF_RANGE, 5, (int32_t)blockIdx.x);
+    return;
+  }
+  const int64_t row_base = ((int64_t)bh * a.n_slots + s0) * L + r0;  // slot s0, row r0
 
+  // 1. slot LSEs of the CTA's rows
+  for (int i = tid; i < ns * ROWS; i += THREADS) {
+    const int t = i / ROWS, r = i - t * ROWS;
+    w_s[t][r] = (r < nrows) ? __ldg(a.part_lse + row_base + (int64_t)t * L + r) : -INFINITY;
+  }
+  __syncthreads();
+  // 2. weights exp(lse_t - lse) and the row LSE
+  if (tid < ROWS) {
+    const int r = tid;
     float M = -INFINITY;
-    for (int t = lane; t < ns; t += 32) M = fmaxf(M, __ldg(lse_p + (int64_t)t * a.L));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int t = 0; t < ns; ++t) M = fmaxf(M, w_s[t][r]);
     const float Ms = (M == -INFINITY) ? 0.f : M;
     float W = 0.f;
-    for (int t = lane; t < ns; t += 32) W += expf(__ldg(lse_p + (int64_t)t * a.L) - Ms);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+    for (int t = 0; t < ns; ++t) {
+      const float e = __expf(w_s[t][r] - Ms);
+      w_s[t][r] = e;
+      W += e;
+    }
     const float invW = W > 0.f ? 1.f / W : 0.f;
-
-    float acc[E];
+    for (int t = 0; t < ns; ++t) w_s[t][r] *= invW;
+    if (r < nrows) a.LSE[(int64_t)bh * a.S + (int64_t)p * L + r0 + r] = (W > 0.f) ? Ms + logf(W) : -INFINITY;
+  }
+  __syncthreads();
+  // 3. stream each slot's contiguous block
+  const float4* src = reinterpret_cast<const float4*>(a.part_o + row_base * D);
+  const int64_t slot_stride = (int64_t)L * V4_PER_ROW;  // float4 per slot
+  float4 acc[PER_THREAD];
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    for (int g = 0; g < ns; g += 32) {
-      const int n = min(32, ns - g);
-      const float wl = (lane < n) ? expf(__ldg(lse_p + (int64_t)(g + lane) * a.L) - Ms) * invW : 0.f;
-      int t = 0;
-      for (; t + 4 <= n; t += 4) {
-        typename V::T v[4];
+  for (int k = 0; k < PER_THREAD; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  int t = 0;
+  for (; t + 2 <= ns; t += 2) {
+    float4 v[2][PER_THREAD];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = __ldcs(o_p + (int64_t)(g + t + q) * o_stride);
+    for (int q = 0; q < 2; ++q)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) V::fma_into(acc, __shfl_sync(0xffffffffu, wl, t + q), v[q]);
+      for (int k = 0; k < PER_THREAD; ++k) {
+        const int idx = tid + k * THREADS;
+        v[q][k] = (idx / V4_PER_ROW < nrows) ? __ldcs(src + (t + q) * slot_stride + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      for (; t < n; ++t) {
-        const typename V::T v = __ldcs(o_p + (int64_t)(g + t) * o_stride);
-        V::fma_into(acc, __shfl_sync(0xffffffffu, wl, t), v);
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int k = 0; k < PER_THREAD; ++k) {
+        const float w = w_s[t + q][(tid + k * THREADS) / V4_PER_ROW];
+        acc[k].x = fmaf(w, v[q][k].x, acc[k].x);
+        acc[k].y = fmaf(w, v[q][k].y, acc[k].y);
+        acc[k].z = fmaf(w, v[q][k].z, acc[k].z);
+        acc[k].w = fmaf(w, v[q][k].w, acc[k].w);
+      }
+  }
+  for (; t < ns; ++t) {
+#pragma unroll
+    for (int k = 0; k < PER_THREAD; ++k) {
+      const int idx = tid + k * THREADS;
+      if (idx / V4_PER_ROW < nrows) {
+        const float4 v = __ldcs(src + t * slot_stride + idx);
+        const float w = w_s[t][idx / V4_PER_ROW];
+        acc[k].x = fmaf(w, v.x, acc[k].x);
+        acc[k].y = fmaf(w, v.y, acc[k].y);
+        acc[k].z = fmaf(w, v.z, acc[k].z);
+        acc[k].w = fmaf(w, v.w, acc[k].w);
       }
     }
-    store_out<E>(reinterpret_cast<OutT*>(a.O) + (bh * a.S + i) * D + lane * E, acc);
-    if (lane == 0) a.LSE[bh * a.S + i] = (W > 0.f) ? Ms + logf(W) : -INFINITY;
+  }
+  // 4. output rows r0 .. r0 + nrows of O[bh, p*L + r, :]
+  OutT* out = reinterpret_cast<OutT*>(a.O) + ((int64_t)bh * a.S + (int64_t)p * L + r0) * D;
+#pragma unroll
+  for (int k = 0; k < PER_THREAD; ++k) {
+    const int idx = tid + k * THREADS;
+    if (idx / V4_PER_ROW < nrows) store4<OutT>(out + (int64_t)idx * 4, acc[k]);
   }
 }
 
 template <int D, typename OutT>
 static int launch(const MergeArgs& a, void* stream, std::string* err) {
-  const int64_t rows = (int64_t)a.B * a.Hq * a.S;
-  if (rows <= 0) return (int)cudaSuccess;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t want = (rows + (THREADS / 32) - 1) / (THREADS / 32);
-  const int64_t cap = (int64_t)(sms > 0 ? sms : 152) * 64;  // enough resident warps, grid-stride beyond
-  const unsigned blocks = (unsigned)(want < cap ? want : cap);
-  merge_kernel<D, OutT><<<blocks, THREADS, 0, (cudaStream_t)stream>>>(a);
+  constexpr int ROWS = 4096 / D;
+  const int64_t n_rblk = (a.L + ROWS - 1) / ROWS;
+  const int64_t blocks = (int64_t)a.B * a.Hq * a.P * n_rblk;
+  if (blocks <= 0) return (int)cudaSuccess;
+  if (blocks > 0x7fffffff || a.L > 0x7fffffff) {
+    *err = "too many merge blocks for one launch";
+    return (int)cudaErrorInvalidConfiguration;
+  }
+  merge_kernel<D, OutT><<<(unsigned)blocks, THREADS, 0, (cudaStream_t)stream>>>(a, (int)n_rblk);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) *err = std::string("merge launch: ") + cudaGetErrorString(e);
   return (int)e;

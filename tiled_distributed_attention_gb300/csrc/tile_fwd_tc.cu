@@ -1,25 +1,36 @@
-// Tile attention forward on the 5th-generation tensor cores (sm_103a): for one work unit
-// (work item = (Q partition p, tile), batch b, query head h, pair of 128-row query tiles) it
-// visits the item's KV partitions in planned order, 128 keys at a time, and writes the
-// partial output O_t = acc / l and lse_t = m + ln l of each query row.
+// Tile attention forward on the 5th-generation tensor cores (sm_103a).
 //
-// The per-block recurrence is the online softmax (running max m_i and running sum l_i) that
-// "环形注意力：突破长序列处理瓶颈的分布式计算范式" describes in §"数值稳定性：Log-Sum-Exp技术的分布式
-// 应用"; the tile/partial structure is Mesh-Attention's ("Mesh-Attention: A New
-// Communication-Efficient Distributed Attention with Improved Data Locality", tutorial
-// §"Mesh-Attention：从一维'环'到二维'网'": each tile's partial results go back to the Q owner).
+// A work unit is (work item = (Q partition p, tile), batch b, query head h, pair of 128-row
+// query tiles of partition p).  For each unit the kernel visits the item's KV partitions in
+// planned order, 128 keys at a time, and writes for every query row the partial output
+// O_t = acc / l and lse_t = m + ln l.  The per-block recurrence is the online softmax with a
+// running maximum m_i and running sum l_i ("环形注意力：突破长序列处理瓶颈的分布式计算范式",
+// §"数值稳定性：Log-Sum-Exp技术的分布式应用"); the tile / partial-output structure is
+// Mesh-Attention's ("Mesh-Attention: A New Communication-Efficient Distributed Attention with
+// Improved Data Locality", tutorial §"Mesh-Attention：从一维'环'到二维'网'": each tile sends its
+// partial results back to the Q owner, which merges them).
 //
-// GB300 mapping (one CTA of 10 warps per unit, 1 CTA per SM):
-//   warp 9      TMA producer: Q tiles once, then K and V blocks through a 2-stage mbarrier ring
-//               (128-byte swizzled boxes of 128 rows x 64 columns).
-//   warp 8      MMA issuer (one thread): S_t = Q_t K^T and O_t += P_t V with tcgen05.mma,
-//               accumulators in tensor memory (TMEM), completion signalled by tcgen05.commit.
-//   warps 0-7   softmax, one warpgroup per query tile: thread i owns row i (TMEM lane i), so
-//               row max and row sum are thread-local; P is written back to TMEM as bf16 in the
-//               columns S occupied and feeds the PV product straight from TMEM.
-// TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 columns each.  The two tiles interleave on
-// the tensor pipe: while softmax 0 works on S_0(j), the pipe runs PV_1(j-1) and S_1(j).
-// O is rescaled only when the running max grows by more than 2^8 (values stay below 256).
+// GB300 mapping: a persistent grid of one CTA per SM; 12 warps = 3 warpgroups.
+//   warp 9      producer: takes the next unit from a global counter (units are numbered in
+//               planned order, item-major), publishes it through a 2-slot ring in shared
+//               memory, then TMA-loads the unit's two Q tiles and streams K and V blocks
+//               (128 rows x 64 columns, 128-byte swizzle) through a 2-stage mbarrier ring.
+//   warp 8      MMA issuer (one thread): S_t = Q_t K^T and O_t += P_t V with
+//               tcgen05.mma.cta_group::1.kind::f16 (M = N = 128, K = 16), fp32 accumulators in
+//               tensor memory, completion signalled with tcgen05.commit.
+//   warps 0-7   softmax, one warpgroup per query tile; thread i owns row i (TMEM lane i), so
+//               row max and row sum are thread-local (3-input max and packed f32x2 FMA / ADD in
+//               independent chains).  P goes back to TMEM as bf16 in the columns S occupied and
+//               feeds the PV product from TMEM.  At the end of a unit the warpgroup copies O_t
+//               out of TMEM into registers, releases it (so the next unit's PV can start), and
+//               stores the rows through a shared-memory stage as whole 128-byte lines.
+//   warps 10-11 idle; warpgroup 2 gives registers to the softmax warpgroups (setmaxnreg).
+// TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  Issue order per block: PV_0(j), S_0(j+1),
+// PV_1(j), S_1(j+1), so the softmax of one tile overlaps the other tile's MMAs.  O is
+// rescaled only when the running max grows by more than 2^8.
+//
+// Every mbarrier wait is bounded: a timeout records MESH_ATTN_ERR_DEVICE_TIMEOUT in the status
+// block, every role of the CTA stops, in-flight copies and MMAs are drained and TMEM is freed.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -34,7 +45,9 @@ namespace tc {
 constexpr int BM = 128;  // query rows per tile = TMEM lanes
 constexpr int BN = 128;  // keys per KV block
 constexpr int NST = 2;   // K/V ring stages
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 384;
+constexpr int SOFTMAX_REGS = 200;  // 2 x 128 x 200 + 128 x 96 <= 384 x 168 registers at launch
+constexpr int OTHER_REGS = 96;
 constexpr int WARP_MMA = 8;
 constexpr int WARP_LOAD = 9;
 constexpr float LOG2_RESCALE = 8.0f;
@@ -50,12 +63,14 @@ struct Layout {
   static constexpr uint32_t Q_OFF = 0;
   static constexpr uint32_t K_OFF = Q_OFF + 2 * TILE;
   static constexpr uint32_t V_OFF = K_OFF + NST * TILE;
-  static constexpr uint32_t BAR_OFF = V_OFF + NST * TILE;
-  // barrier indices
-  static constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = B_KFULL + NST, B_VFULL = B_KEMPTY + NST,
-                       B_VEMPTY = B_VFULL + NST, B_SFULL = B_VEMPTY + NST, B_PFULL = B_SFULL + 2,
-                       B_OFINAL = B_PFULL + 2, NBARS = B_OFINAL + 1;
-  static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;
+  static constexpr uint32_t EPI_OFF = V_OFF + NST * TILE;  // 8 softmax warps x 32 x 32 fp32
+  static constexpr uint32_t BAR_OFF = EPI_OFF + 8 * 4096;
+  static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = B_KFULL + NST,
+                       B_VFULL = B_KEMPTY + NST, B_VEMPTY = B_VFULL + NST, B_SFULL = B_VEMPTY + NST,
+                       B_PFULL = B_SFULL + 2, B_OFINAL = B_PFULL + 2, B_OFREE = B_OFINAL + 2,
+                       B_UFULL = B_OFREE + 2, B_UEMPTY = B_UFULL + 2, B_DRAIN = B_UEMPTY + 2,
+                       NBARS = B_DRAIN + 1;
+  static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag, unit ring[2]
   static constexpr uint32_t TOTAL = MISC_OFF + 16;
   static constexpr uint32_t ALLOC = TOTAL + 1024;
 };
@@ -66,14 +81,44 @@ struct Params {
   float* part_o;
   float* part_lse;
   int32_t* status;
+  uint32_t* counter;
   int64_t S, L;
-  int32_t B, Hq, Hkv, P, n_items, n_slots, n_pairs, causal;
+  int32_t B, Hq, Hkv, P, n_items, n_slots, n_pairs, n_units, causal;
   float scale_log2;
   int64_t wait_limit_ns;
 };
 
-// Number of 128-key blocks of KV partition k visited for Q partition p by a unit whose last
-// query tile is a_max (tile index within the partition).
+// What every role derives from a unit index.
+struct Unit {
+  int b, h, qp;
+  DevItem it;
+  bool ok;      // item indices in range
+  int ntiles;   // 1 or 2 query tiles (2 unless the partition has an odd number of tiles)
+  int a0;       // first query tile index within the partition
+  int a_max;    // last query tile index
+  int nb;       // 128-key blocks per KV partition
+};
+
+__device__ __forceinline__ Unit decode(int u, const Params& prm) {
+  Unit x;
+  x.qp = u % prm.n_pairs;
+  u /= prm.n_pairs;
+  x.h = u % prm.Hq;
+  u /= prm.Hq;
+  x.b = u % prm.B;
+  const int item = u / prm.B;
+  x.it = prm.items[item];
+  x.ok = x.it.p >= 0 && x.it.p < prm.P && x.it.slot >= 0 && x.it.slot < prm.n_slots && x.it.n_kv >= 1 &&
+         x.it.kv_off >= 0;
+  x.nb = (int)((prm.L + BN - 1) / BN);
+  x.a0 = 2 * x.qp;
+  x.ntiles = ((int64_t)(x.a0 + 1) * BM < prm.L) ? 2 : 1;
+  x.a_max = x.a0 + x.ntiles - 1;
+  return x;
+}
+
+// 128-key blocks of KV partition k visited for Q partition p by a unit whose last query tile
+// is a_max: only the causal diagonal partition is cut short.
 __device__ __forceinline__ int blocks_of(int k, int p, int causal, int nb, int a_max) {
   return (causal && k == p) ? min(nb, a_max + 1) : nb;
 }
@@ -85,23 +130,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   using Ly = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sb = (raw + 1023u) & ~1023u;  // 1024-aligned base (128B swizzle atoms)
+  const uint32_t sb = (raw + 1023u) & ~1023u;  // 1024-aligned base (128-byte swizzle atoms)
   uint8_t* smem = smem_raw + (sb - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) { return sb + Ly::BAR_OFF + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::MISC_OFF);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + Ly::MISC_OFF + 4);
-
-  // ---- unit decode: (item, b, h, pair) with the pair fastest
-  int64_t u = blockIdx.x;
-  const int qp = (int)(u % prm.n_pairs); u /= prm.n_pairs;
-  const int h = (int)(u % prm.Hq); u /= prm.Hq;
-  const int b = (int)(u % prm.B);
-  const int item_idx = (int)(u / prm.B);
-  const int unit = (int)blockIdx.x;
+  volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(smem + Ly::MISC_OFF + 8);
+  const int64_t L = prm.L;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Ly::B_QFULL), 1);
+    mbar_init(bar(Ly::B_QEMPTY), 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(bar(Ly::B_KFULL + s), 1);
       mbar_init(bar(Ly::B_KEMPTY + s), 1);
@@ -111,8 +151,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(Ly::B_SFULL + t), 1);
       mbar_init(bar(Ly::B_PFULL + t), BM);
+      mbar_init(bar(Ly::B_OFINAL + t), 1);
+      mbar_init(bar(Ly::B_OFREE + t), BM);
+      mbar_init(bar(Ly::B_UFULL + t), 1);
+      mbar_init(bar(Ly::B_UEMPTY + t), 1 + 8);  // MMA thread + one lane of each softmax warp
     }
-    mbar_init(bar(Ly::B_OFINAL), 1);
+    mbar_init(bar(Ly::B_DRAIN), 1);
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0) ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -131,41 +175,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const DevItem it = prm.items[item_idx];
-  const int64_t L = prm.L;
-  const bool item_ok = it.p >= 0 && it.p < prm.P && it.slot >= 0 && it.slot < prm.n_slots && it.n_kv >= 1 &&
-                       it.kv_off >= 0;
-  if (!item_ok && threadIdx.x == 0) record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_ITEM, unit);
-  const bool run = item_ok && (*abort_flag == 0);
-  const int p = it.p;
-  const int nb = (int)((L + BN - 1) / BN);
-  const int a0 = 2 * qp;
-  const bool has1 = (int64_t)(a0 + 1) * BM < L;
-  const int ntiles = has1 ? 2 : 1;
-  const int a_max = a0 + ntiles - 1;
-  const int hk = h / (prm.Hq / prm.Hkv);
-  const int32_t* kvl = prm.kv_list + it.kv_off;
-
-  if (run && warp < 8) {
+  if (warp < 8) {
     // ================================================================ softmax warpgroups
+    regs_inc<SOFTMAX_REGS>();
     const int t = warp >> 2;
     const int wq = warp & 3;
     const int row = wq * 32 + lane;  // row within the tile = TMEM lane
-    const int a_t = a0 + t;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const uint32_t tm_s = tmem + lane_base + (uint32_t)(t * 128);
     const uint32_t tm_o = tmem + lane_base + 256u + (uint32_t)(t * 128);
-    float m_used = -INFINITY, l_sum = 0.f;
+    float* epi = reinterpret_cast<float*>(smem + Ly::EPI_OFF + (uint32_t)warp * 4096u);
+    int nu = 0, cnt = 0, uses = 0;
     bool ok = true;
-    if (t < ntiles) {
-      int j = 0;
-      for (int ki = 0; ki < it.n_kv && ok; ++ki) {
+    while (ok) {
+      const int slot = nu & 1;
+      ok = mbar_wait(bar(Ly::B_UFULL + slot), (uint32_t)((nu >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                     ROLE_SOFTMAX, -1);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const int u = unit_ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Ly::B_UEMPTY + slot));
+      ++nu;
+      if (u < 0) break;
+      const Unit x = decode(u, prm);
+      if (!x.ok) break;
+      if (t >= x.ntiles) continue;
+      const int p = x.it.p;
+      const int a_t = x.a0 + t;
+      const int32_t* kvl = prm.kv_list + x.it.kv_off;
+      float m_used = -INFINITY, l_sum = 0.f;
+      for (int ki = 0; ki < x.it.n_kv && ok; ++ki) {
         const int k = __ldg(kvl + ki);
         const bool diag = prm.causal && k == p;
-        const int nbk = blocks_of(k, p, prm.causal, nb, a_max);
-        for (int jb = 0; jb < nbk; ++jb, ++j) {
-          ok = mbar_wait(bar(Ly::B_SFULL + t), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status,
-                         ROLE_SOFTMAX, unit);
+        const int nbk = blocks_of(k, p, prm.causal, x.nb, x.a_max);
+        for (int jb = 0; jb < nbk; ++jb, ++cnt) {
+          ok = mbar_wait(bar(Ly::B_SFULL + t), (uint32_t)(cnt & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                         ROLE_SOFTMAX, u);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
@@ -173,19 +219,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int c = 0; c < BN; c += 32) tmem_ld32(tm_s + (uint32_t)c, s + c);
           tc_wait_ld();
-          const int64_t kv_valid = min((int64_t)BN, L - (int64_t)jb * BN);
+          // mask: causal diagonal block (key column > query row) and keys past the partition
+          const int kv_valid = (int)min((int64_t)BN, L - (int64_t)jb * BN);
           int lim = BN - 1;
           if (diag) lim = (jb < a_t) ? BN - 1 : (jb == a_t ? row : -1);
-          lim = min(lim, (int)kv_valid - 1);
+          lim = min(lim, kv_valid - 1);
           if (lim < BN - 1) {
 #pragma unroll
             for (int c = 0; c < BN; ++c)
               if (c > lim) s[c] = -INFINITY;
           }
-          float mx = s[0];
+          // row max: four independent chains of 3-input max
+          float mc[4];
 #pragma unroll
-          for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
-          const float m_new = mx * prm.scale_log2;
+          for (int q = 0; q < 4; ++q) {
+            float v = max3f(s[32 * q], s[32 * q + 1], s[32 * q + 2]);
+#pragma unroll
+            for (int i = 3; i + 1 < 32; i += 2) v = max3f(v, s[32 * q + i], s[32 * q + i + 1]);
+            mc[q] = fmaxf(v, s[32 * q + 31]);
+          }
+          const float m_new = fmaxf(max3f(mc[0], mc[1], mc[2]), mc[3]) * prm.scale_log2;
           float factor = 1.f;
           if (m_new > -INFINITY) {
             if (m_used == -INFINITY) {
@@ -196,8 +249,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           if (__any_sync(0xffffffffu, factor != 1.f)) {
-            // O_t already holds every earlier PV product: S_t(j) was issued after PV_t(j-1)
-            // and its completion covers all earlier tensor-core work of the issuing thread.
+            // O_t holds every earlier PV product of this unit: S_t(j) was issued after
+            // PV_t(j-1) and its completion covers all earlier tensor-core work.
             l_sum *= factor;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
@@ -211,16 +264,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-          float sum = 0.f;
+          // p = 2^(s * scale * log2 e - m): two elements per FMA, four independent sum chains
+          const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2);
+          const uint64_t nm2 = f2_pack(-mref, -mref);
+          uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
           uint32_t pk[BN / 2];
 #pragma unroll
           for (int c = 0; c < BN / 2; ++c) {
-            const float p0 = fast_exp2(fmaf(s[2 * c], prm.scale_log2, -mref));
-            const float p1 = fast_exp2(fmaf(s[2 * c + 1], prm.scale_log2, -mref));
-            sum += p0 + p1;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sc2, nm2), x0, x1);
+            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            acc2[c & 3] = f2_add(acc2[c & 3], f2_pack(p0, p1));
             pk[c] = pack_bf16x2(p0, p1);
           }
-          l_sum += sum;
+          float sa, sb2;
+          f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), sa, sb2);
+          l_sum += sa + sb2;
           tmem_st32(tm_s, pk);
           tmem_st32(tm_s + 32u, pk + 32);
           tc_wait_st();
@@ -228,36 +287,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive(bar(Ly::B_PFULL + t));
         }
       }
-      if (ok) {
-        ok = mbar_wait(bar(Ly::B_OFINAL), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_SOFTMAX, unit);
-        ok = __all_sync(0xffffffffu, ok);
-      }
-      if (ok) {
-        tc_fence_after();
-        const int64_t row_local = (int64_t)a_t * BM + row;
-        const bool valid = row_local < L;
-        const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-        const int64_t prow = (((int64_t)b * prm.Hq + h) * prm.n_slots + it.slot) * L + row_local;
-        float* dst = prm.part_o + prow * D;
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          float o[32];
-          tmem_ld32(tm_o + (uint32_t)c, o);
-          tc_wait_ld();
-          if (valid) {
+      if (!ok) break;
+      // ---- epilogue: copy O_t out of TMEM, release it, store through the shared stage
+      ok = mbar_wait(bar(Ly::B_OFINAL + t), (uint32_t)(uses & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                     ROLE_SOFTMAX, u);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float o[D];
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(dst + c + e) =
-                  make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
-          }
+      for (int c = 0; c < D; c += 32) tmem_ld32(tm_o + (uint32_t)c, o + c);
+      tc_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(Ly::B_OFREE + t));
+      ++uses;
+      const int64_t row_local = (int64_t)a_t * BM + row;
+      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      const int64_t prow = (((int64_t)x.b * prm.Hq + x.h) * prm.n_slots + x.it.slot) * L + row_local;
+      const int64_t wrow0 = row_local - lane;          // warp's first row in the partition
+      float* dst0 = prm.part_o + (prow - lane) * D;    // that row in the slot
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        // 32 rows x 32 columns: 16-byte chunks swizzled by row, read back 4 rows per store
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(epi + lane * 32 + ((q ^ (lane & 7)) * 4)) =
+              make_float4(o[c + 4 * q] * inv, o[c + 4 * q + 1] * inv, o[c + 4 * q + 2] * inv,
+                          o[c + 4 * q + 3] * inv);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = i * 4 + (lane >> 3), qq = lane & 7;
+          const float4 v = *reinterpret_cast<const float4*>(epi + r * 32 + ((qq ^ (r & 7)) * 4));
+          if (wrow0 + r < L) *reinterpret_cast<float4*>(dst0 + (int64_t)r * D + c + qq * 4) = v;
         }
-        if (valid)
-          prm.part_lse[prow] = l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+        __syncwarp();
       }
+      if (row_local < L)
+        prm.part_lse[prow] = l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
     }
-  } else if (run && warp == WARP_MMA) {
-    // ================================================================ MMA issuer
-    if (lane == 0) {
+  } else {
+    regs_dec<OTHER_REGS>();
+    if (warp == WARP_MMA && lane == 0) {
+      // ================================================================ MMA issuer
       const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false);
       const uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
       auto q_addr = [&](int t) { return sb + Ly::Q_OFF + (uint32_t)t * Ly::TILE; };
@@ -267,104 +339,153 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       auto kmaj = [&](uint32_t base, int kk) {
         return smem_desc_sw128(base + (uint32_t)(kk >> 2) * Ly::BOX + (uint32_t)(kk & 3) * 32u, 16u, 1024u);
       };
-      // MN-major V: K-step kk covers rows 16kk..16kk+15 (2 swizzle atoms of 8 rows); the
+      // MN-major V: K-step kk covers key rows 16kk..16kk+15 (two 8-row swizzle atoms); the
       // second 64-column half of d is the next box (leading byte offset)
       auto vdesc = [&](int s, int kk) { return smem_desc_sw128(v_addr(s) + (uint32_t)kk * 2048u, Ly::BOX, 1024u); };
-      int NB = 0;
-      for (int ki = 0; ki < it.n_kv; ++ki) NB += blocks_of(__ldg(kvl + ki), p, prm.causal, nb, a_max);
-      bool ok = mbar_wait(bar(Ly::B_QFULL), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, unit);
-      if (ok) ok = mbar_wait(bar(Ly::B_KFULL + 0), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, unit);
-      if (ok) {
+      auto issue_s = [&](int t, int stage) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_ss(tmem + (uint32_t)(t * 128), kmaj(q_addr(t), kk), kmaj(k_addr(stage), kk), idesc_qk, kk > 0);
+        tc_commit(bar(Ly::B_SFULL + t));
+      };
+      int nu = 0, nblk = 0;
+      int cnt[2] = {0, 0}, uses[2] = {0, 0};
+      bool ok = true;
+      while (ok) {
+        const int slot = nu & 1;
+        ok = mbar_wait(bar(Ly::B_UFULL + slot), (uint32_t)((nu >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                       ROLE_MMA, -1);
+        if (!ok) break;
+        const int u = unit_ring[slot];
+        mbar_arrive(bar(Ly::B_UEMPTY + slot));
+        const int uidx = nu++;
+        if (u < 0) break;
+        const Unit x = decode(u, prm);
+        if (!x.ok) break;
+        const int32_t* kvl = prm.kv_list + x.it.kv_off;
+        int NB = 0;
+        for (int ki = 0; ki < x.it.n_kv; ++ki) NB += blocks_of(__ldg(kvl + ki), x.it.p, prm.causal, x.nb, x.a_max);
+        ok = mbar_wait(bar(Ly::B_QFULL), (uint32_t)(uidx & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, u);
+        if (ok)
+          ok = mbar_wait(bar(Ly::B_KFULL + nblk % NST), (uint32_t)((nblk / NST) & 1), prm.wait_limit_ns, abort_flag,
+                         prm.status, ROLE_MMA, u);
+        if (!ok) break;
         tc_fence_after();
-        for (int t = 0; t < ntiles; ++t) {
+        for (int t = 0; t < x.ntiles; ++t) issue_s(t, nblk % NST);
+        if (NB == 1) tc_commit(bar(Ly::B_QEMPTY));
+        tc_commit(bar(Ly::B_KEMPTY + nblk % NST));
+        for (int j = 0; j < NB && ok; ++j) {
+          const int g = nblk + j;
+          const int st = g % NST;
+          ok = mbar_wait(bar(Ly::B_VFULL + st), (uint32_t)((g / NST) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                         ROLE_MMA, u);
+          for (int t = 0; t < x.ntiles && ok; ++t) {
+            ok = mbar_wait(bar(Ly::B_PFULL + t), (uint32_t)(cnt[t] & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                           ROLE_MMA, u);
+            if (ok && j == 0 && uses[t] > 0)  // the previous unit's epilogue has copied O_t out
+              ok = mbar_wait(bar(Ly::B_OFREE + t), (uint32_t)((uses[t] - 1) & 1), prm.wait_limit_ns, abort_flag,
+                             prm.status, ROLE_MMA, u);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t tm_p = tmem + (uint32_t)(t * 128);
+            const uint32_t tm_o = tmem + 256u + (uint32_t)(t * 128);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            tc_mma_ss(tmem + (uint32_t)(t * 128), kmaj(q_addr(t), kk), kmaj(k_addr(0), kk), idesc_qk, kk > 0);
-          tc_commit(bar(Ly::B_SFULL + t));
-        }
-        tc_commit(bar(Ly::B_KEMPTY + 0));
-      }
-      for (int j = 0; j < NB && ok; ++j) {
-        const int st = j % NST;
-        const uint32_t ph = (uint32_t)((j / NST) & 1);
-        ok = mbar_wait(bar(Ly::B_VFULL + st), ph, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, unit);
-        for (int t = 0; t < ntiles && ok; ++t) {
-          ok = mbar_wait(bar(Ly::B_PFULL + t), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status,
-                         ROLE_MMA, unit);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t tm_p = tmem + (uint32_t)(t * 128);
-          const uint32_t tm_o = tmem + 256u + (uint32_t)(t * 128);
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            tc_mma_ts(tm_o, tm_p + (uint32_t)(kk * 8), vdesc(st, kk), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-          if (j + 1 < NB) {
-            const int sn = (j + 1) % NST;
-            if (t == 0) {
-              ok = mbar_wait(bar(Ly::B_KFULL + sn), (uint32_t)(((j + 1) / NST) & 1), prm.wait_limit_ns,
-                             abort_flag, prm.status, ROLE_MMA, unit);
-              if (!ok) break;
-              tc_fence_after();
+            for (int kk = 0; kk < BN / 16; ++kk)
+              tc_mma_ts(tm_o, tm_p + (uint32_t)(kk * 8), vdesc(st, kk), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            ++cnt[t];
+            if (j + 1 < NB) {
+              const int sn = (g + 1) % NST;
+              if (t == 0) {
+                ok = mbar_wait(bar(Ly::B_KFULL + sn), (uint32_t)(((g + 1) / NST) & 1), prm.wait_limit_ns, abort_flag,
+                               prm.status, ROLE_MMA, u);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              issue_s(t, sn);
             }
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              tc_mma_ss(tm_p, kmaj(q_addr(t), kk), kmaj(k_addr(sn), kk), idesc_qk, kk > 0);
-            tc_commit(bar(Ly::B_SFULL + t));
           }
+          if (!ok) break;
+          if (j + 1 < NB) tc_commit(bar(Ly::B_KEMPTY + (g + 1) % NST));
+          if (j + 2 == NB) tc_commit(bar(Ly::B_QEMPTY));  // the unit's last S products are issued
+          tc_commit(bar(Ly::B_VEMPTY + st));
         }
         if (!ok) break;
-        if (j + 1 < NB) tc_commit(bar(Ly::B_KEMPTY + (j + 1) % NST));
-        tc_commit(bar(Ly::B_VEMPTY + st));
+        for (int t = 0; t < x.ntiles; ++t) {
+          tc_commit(bar(Ly::B_OFINAL + t));
+          ++uses[t];
+        }
+        nblk += NB;
       }
-      // o_final completes when every MMA above has: the softmax epilogue reads O after it, and
-      // it is the exit-path drain before TMEM is freed.
-      tc_commit(bar(Ly::B_OFINAL));
-      mbar_drain(bar(Ly::B_OFINAL), 0u, DRAIN_NS);
-    }
-  } else if (run && warp == WARP_LOAD) {
-    // ================================================================ TMA producer
-    if (lane == 0) {
-      const int64_t qrow0 = ((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + (int64_t)a0 * BM;
-      mbar_expect_tx(bar(Ly::B_QFULL), (uint32_t)ntiles * Ly::TILE);
-      for (int t = 0; t < ntiles; ++t)
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(sb + Ly::Q_OFF + (uint32_t)t * Ly::TILE + (uint32_t)c * Ly::BOX, &tmQ, c * 64,
-                      (int32_t)(qrow0 + (int64_t)t * BM), bar(Ly::B_QFULL));
-      const int64_t kvbase = ((int64_t)b * prm.Hkv + hk) * prm.S;
-      int nk = 0, nv = 0;  // K and V block loads issued
-      bool ok = true;
-      for (int ki = 0; ki < it.n_kv && ok; ++ki) {
-        const int k = __ldg(kvl + ki);
-        if (k < 0 || k >= prm.P) {
-          record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_LOAD, unit);
+      // exit-path drain: every MMA issued completes before TMEM is freed
+      tc_commit(bar(Ly::B_DRAIN));
+      mbar_drain(bar(Ly::B_DRAIN), 0u, DRAIN_NS);
+    } else if (warp == WARP_LOAD && lane == 0) {
+      // ================================================================ producer
+      int nu = 0, nq = 0, nk = 0, nv = 0;
+      bool ok = *abort_flag == 0;
+      while (ok) {
+        const int slot = nu & 1;
+        ok = mbar_wait(bar(Ly::B_UEMPTY + slot), (uint32_t)(((nu >> 1) & 1) ^ 1), prm.wait_limit_ns, abort_flag,
+                       prm.status, ROLE_LOAD, -1);
+        if (!ok) break;
+        int u = (int)atomicAdd(prm.counter, 1u);
+        if (u >= prm.n_units) u = -1;
+        unit_ring[slot] = u;
+        mbar_arrive(bar(Ly::B_UFULL + slot));
+        ++nu;
+        if (u < 0) break;
+        const Unit x = decode(u, prm);
+        if (!x.ok) {
+          record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_ITEM, u);
           *abort_flag = 1;
           break;
         }
-        const int nbk = blocks_of(k, p, prm.causal, nb, a_max);
-        for (int jb = 0; jb < nbk; ++jb) {
-          const int st = nk % NST;
-          const uint32_t ph = (uint32_t)((nk / NST) & 1);
-          const int32_t krow = (int32_t)(kvbase + (int64_t)k * L + (int64_t)jb * BN);
-          ok = mbar_wait(bar(Ly::B_KEMPTY + st), ph ^ 1u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_LOAD,
-                         unit);
-          if (!ok) break;
-          mbar_expect_tx(bar(Ly::B_KFULL + st), Ly::TILE);
+        // Q tiles: the previous unit's last S products must be done with the Q buffer
+        ok = mbar_wait(bar(Ly::B_QEMPTY), (uint32_t)((nq & 1) ^ 1), prm.wait_limit_ns, abort_flag, prm.status,
+                       ROLE_LOAD, u);
+        if (!ok) break;
+        const int64_t qrow0 = ((int64_t)x.b * prm.Hq + x.h) * prm.S + (int64_t)x.it.p * L + (int64_t)x.a0 * BM;
+        mbar_expect_tx(bar(Ly::B_QFULL), (uint32_t)x.ntiles * Ly::TILE);
+        for (int t = 0; t < x.ntiles; ++t)
           for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(sb + Ly::K_OFF + (uint32_t)st * Ly::TILE + (uint32_t)c * Ly::BOX, &tmK, c * 64, krow,
-                        bar(Ly::B_KFULL + st));
-          ++nk;
-          ok = mbar_wait(bar(Ly::B_VEMPTY + st), ph ^ 1u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_LOAD,
-                         unit);
-          if (!ok) break;
-          mbar_expect_tx(bar(Ly::B_VFULL + st), Ly::TILE);
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_2d(sb + Ly::V_OFF + (uint32_t)st * Ly::TILE + (uint32_t)c * Ly::BOX, &tmV, c * 64, krow,
-                        bar(Ly::B_VFULL + st));
-          ++nv;
+            tma_load_2d(sb + Ly::Q_OFF + (uint32_t)t * Ly::TILE + (uint32_t)c * Ly::BOX, &tmQ, c * 64,
+                        (int32_t)(qrow0 + (int64_t)t * BM), bar(Ly::B_QFULL));
+        ++nq;
+        const int hk = x.h / (prm.Hq / prm.Hkv);
+        const int64_t kvbase = ((int64_t)x.b * prm.Hkv + hk) * prm.S;
+        const int32_t* kvl = prm.kv_list + x.it.kv_off;
+        for (int ki = 0; ki < x.it.n_kv && ok; ++ki) {
+          const int k = __ldg(kvl + ki);
+          if (k < 0 || k >= prm.P) {
+            record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_LOAD, u);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          const int nbk = blocks_of(k, x.it.p, prm.causal, x.nb, x.a_max);
+          for (int jb = 0; jb < nbk; ++jb) {
+            const int st = nk % NST;
+            const uint32_t ph = (uint32_t)((nk / NST) & 1);
+            const int32_t krow = (int32_t)(kvbase + (int64_t)k * L + (int64_t)jb * BN);
+            ok = mbar_wait(bar(Ly::B_KEMPTY + st), ph ^ 1u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_LOAD, u);
+            if (!ok) break;
+            mbar_expect_tx(bar(Ly::B_KFULL + st), Ly::TILE);
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_2d(sb + Ly::K_OFF + (uint32_t)st * Ly::TILE + (uint32_t)c * Ly::BOX, &tmK, c * 64, krow,
+                          bar(Ly::B_KFULL + st));
+            ++nk;
+            ok = mbar_wait(bar(Ly::B_VEMPTY + st), ph ^ 1u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_LOAD, u);
+            if (!ok) break;
+            mbar_expect_tx(bar(Ly::B_VFULL + st), Ly::TILE);
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_2d(sb + Ly::V_OFF + (uint32_t)st * Ly::TILE + (uint32_t)c * Ly::BOX, &tmV, c * 64, krow,
+                          bar(Ly::B_VFULL + st));
+            ++nv;
+          }
         }
       }
-      // drain: every load issued must land before the CTA exits (the last NST of each ring)
-      mbar_drain(bar(Ly::B_QFULL), 0u, DRAIN_NS);
+      // exit-path drain: every load issued lands before the CTA exits
+      if (nq > 0) mbar_drain(bar(Ly::B_QFULL), (uint32_t)((nq - 1) & 1), DRAIN_NS);
       for (int jj = (nk > NST ? nk - NST : 0); jj < nk; ++jj)
         mbar_drain(bar(Ly::B_KFULL + jj % NST), (uint32_t)((jj / NST) & 1), DRAIN_NS);
       for (int jj = (nv > NST ? nv - NST : 0); jj < nv; ++jj)
@@ -438,6 +559,7 @@ static int launch(const TileArgs& a, void* stream, std::string* err) {
   prm.part_o = a.part_o;
   prm.part_lse = a.part_lse;
   prm.status = a.status;
+  prm.counter = a.counter;
   prm.S = a.S;
   prm.L = a.L;
   prm.B = a.B;
@@ -447,16 +569,25 @@ static int launch(const TileArgs& a, void* stream, std::string* err) {
   prm.n_items = a.n_items;
   prm.n_slots = a.n_slots;
   prm.n_pairs = (int32_t)n_pairs;
+  prm.n_units = (int32_t)units;
   prm.causal = a.causal;
   prm.scale_log2 = a.scale_log2;
   prm.wait_limit_ns = a.wait_limit_ns;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    *err = std::string("device query: ") + cudaGetErrorString(e);
+    return (int)e;
+  }
   auto kern = tile_fwd_tc_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<D>::ALLOC);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<D>::ALLOC);
   if (e != cudaSuccess) {
     *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
     return (int)e;
   }
-  kern<<<dim3((unsigned)units), dim3(NUM_THREADS), Layout<D>::ALLOC, (cudaStream_t)stream>>>(mq, mk, mv, prm);
+  const unsigned grid = (unsigned)(units < sms ? units : sms);  // persistent: one CTA per SM
+  kern<<<dim3(grid), dim3(NUM_THREADS), Layout<D>::ALLOC, (cudaStream_t)stream>>>(mq, mk, mv, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) *err = std::string("tile_fwd_tc launch: ") + cudaGetErrorString(e);
   return (int)e;
