@@ -110,6 +110,21 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(x: float, device) -> float:
+    """Largest value of x over all ranks (the job's time is its slowest rank's)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def job_throughput(world: int, flops_per_rank: float, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own copy of the workload (weak scaling)."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -246,14 +261,10 @@ def main():
     total_ms = t_start.elapsed_time(t_end)
     tile_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     merge_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = t.item()
+    total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
     flops = algorithmic_flops(w)
-    value = ws * flops / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(ws, flops, ms_per_step)
 
     # end to end through the public call, host buffers in pinned memory
     e2e = None
@@ -281,13 +292,9 @@ def main():
         torch.cuda.synchronize()
         barrier()
         e_ms = e0.elapsed_time(e1) / n_e2e
-        if ws > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = t.item()
+        e_ms = max_over_ranks(e_ms, dev)
         es = q.element_size()
-        e2e = {"value": ws * flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+        e2e = {"value": job_throughput(ws, flops, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int((q.numel() + k.numel() + v.numel()) * es),
                "d2h_bytes_per_step": int(O.numel() * O.element_size() + LSE.numel() * 4),
                "ms_per_step": e_ms, "steps": n_e2e}
