@@ -330,23 +330,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     regs_dec<OTHER_REGS>();
     if (warp == WARP_MMA && lane == 0) {
       // ================================================================ MMA issuer
-      const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false);
-      const uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
-      auto q_addr = [&](int t) { return sb + Ly::Q_OFF + (uint32_t)t * Ly::TILE; };
-      auto k_addr = [&](int s) { return sb + Ly::K_OFF + (uint32_t)s * Ly::TILE; };
-      auto v_addr = [&](int s) { return sb + Ly::V_OFF + (uint32_t)s * Ly::TILE; };
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
+      // Base descriptors are built once; per instruction only the start-address field (the
+      // low 14 bits, address / 16) advances by a compile-time offset.  Shared addresses stay
+      // below 256 KB, so the addition never carries out of that field.  Keeping the issuing
+      // thread's work per MMA to a few independent adds is what lets one thread keep the
+      // tensor pipe fed.
+      const uint64_t q_desc0 = smem_desc_sw128(sb + Ly::Q_OFF, 16u, 1024u);
+      const uint64_t k_desc0 = smem_desc_sw128(sb + Ly::K_OFF, 16u, 1024u);
+      const uint64_t v_desc0 = smem_desc_sw128(sb + Ly::V_OFF, Ly::BOX, 1024u);
+      constexpr uint64_t TILE16 = Ly::TILE >> 4, BOX16 = Ly::BOX >> 4;
       // K-major operand (Q or K): K-step kk of 16 elements sits in box kk/4 at byte 32*(kk%4)
-      auto kmaj = [&](uint32_t base, int kk) {
-        return smem_desc_sw128(base + (uint32_t)(kk >> 2) * Ly::BOX + (uint32_t)(kk & 3) * 32u, 16u, 1024u);
-      };
-      // MN-major V: K-step kk covers key rows 16kk..16kk+15 (two 8-row swizzle atoms); the
-      // second 64-column half of d is the next box (leading byte offset)
-      auto vdesc = [&](int s, int kk) { return smem_desc_sw128(v_addr(s) + (uint32_t)kk * 2048u, Ly::BOX, 1024u); };
+      auto kmaj_off = [](int kk) { return (uint64_t)((kk >> 2) * BOX16 + (kk & 3) * 2); };
+      // MN-major V: K-step kk covers key rows 16kk..16kk+15 (two 8-row swizzle atoms, 2048
+      // bytes); the second 64-column half of d is the next box (leading byte offset)
       auto issue_s = [&](int t, int stage) {
+        const uint64_t qd = q_desc0 + (uint64_t)t * TILE16;
+        const uint64_t kd = k_desc0 + (uint64_t)stage * TILE16;
+        const uint32_t d_tm = tmem + (uint32_t)(t * 128);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss(tmem + (uint32_t)(t * 128), kmaj(q_addr(t), kk), kmaj(k_addr(stage), kk), idesc_qk, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) tc_mma_ss(d_tm, qd + kmaj_off(kk), kd + kmaj_off(kk), idesc_qk, kk > 0);
         tc_commit(bar(Ly::B_SFULL + t));
+      };
+      auto issue_pv = [&](int t, int stage, bool first) {
+        const uint64_t vd = v_desc0 + (uint64_t)stage * TILE16;
+        const uint32_t tm_p = tmem + (uint32_t)(t * 128);
+        const uint32_t tm_o = tmem + 256u + (uint32_t)(t * 128);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          tc_mma_ts(tm_o, tm_p + (uint32_t)(kk * 8), vd + (uint64_t)(kk * 128), idesc_pv, (!first || kk > 0) ? 1u : 0u);
       };
       int nu = 0, nblk = 0;
       int cnt[2] = {0, 0}, uses[2] = {0, 0};
@@ -387,11 +400,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              prm.status, ROLE_MMA, u);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t tm_p = tmem + (uint32_t)(t * 128);
-            const uint32_t tm_o = tmem + 256u + (uint32_t)(t * 128);
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              tc_mma_ts(tm_o, tm_p + (uint32_t)(kk * 8), vdesc(st, kk), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            issue_pv(t, st, j == 0);
             ++cnt[t];
             if (j + 1 < NB) {
               const int sn = (g + 1) % NST;
