@@ -402,6 +402,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             issue_pv(t, st, j == 0);
             ++cnt[t];
+            if (j + 1 == NB) {  // tile t's last product of the unit: its epilogue may start
+              tc_commit(bar(Ly::B_OFINAL + t));
+              ++uses[t];
+            }
             if (j + 1 < NB) {
               const int sn = (g + 1) % NST;
               if (t == 0) {
@@ -419,10 +423,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_commit(bar(Ly::B_VEMPTY + st));
         }
         if (!ok) break;
-        for (int t = 0; t < x.ntiles; ++t) {
-          tc_commit(bar(Ly::B_OFINAL + t));
-          ++uses[t];
-        }
         nblk += NB;
       }
       // exit-path drain: every MMA issued completes before TMEM is freed
@@ -432,22 +432,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ================================================================ producer
       int nu = 0, nq = 0, nk = 0, nv = 0;
       bool ok = *abort_flag == 0;
-      while (ok) {
+      // take the next unit from the global counter and publish it to the consumers' ring
+      auto publish = [&]() -> int {
         const int slot = nu & 1;
         ok = mbar_wait(bar(Ly::B_UEMPTY + slot), (uint32_t)(((nu >> 1) & 1) ^ 1), prm.wait_limit_ns, abort_flag,
                        prm.status, ROLE_LOAD, -1);
-        if (!ok) break;
-        int u = (int)atomicAdd(prm.counter, 1u);
-        if (u >= prm.n_units) u = -1;
-        unit_ring[slot] = u;
+        if (!ok) return -1;
+        int v = (int)atomicAdd(prm.counter, 1u);
+        if (v >= prm.n_units) v = -1;
+        unit_ring[slot] = v;
         mbar_arrive(bar(Ly::B_UFULL + slot));
         ++nu;
-        if (u < 0) break;
+        return v;
+      };
+      int u = ok ? publish() : -1;
+      while (ok && u >= 0) {
         const Unit x = decode(u, prm);
         if (!x.ok) {
           record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_ITEM, u);
           *abort_flag = 1;
           break;
+        }
+        // publish the following unit now and pull its Q tiles and first K/V block into L2, so
+        // the unit boundary does not wait on DRAM
+        const int un = publish();
+        if (!ok) break;
+        if (un >= 0) {
+          const Unit xn = decode(un, prm);
+          if (xn.ok) {
+            const int64_t qn = ((int64_t)xn.b * prm.Hq + xn.h) * prm.S + (int64_t)xn.it.p * L + (int64_t)xn.a0 * BM;
+            for (int t = 0; t < xn.ntiles; ++t)
+              for (int c = 0; c < D / 64; ++c) tma_prefetch_l2_2d(&tmQ, c * 64, (int32_t)(qn + (int64_t)t * BM));
+            const int kn = __ldg(prm.kv_list + xn.it.kv_off);
+            if (kn >= 0 && kn < prm.P) {
+              const int64_t krn = ((int64_t)xn.b * prm.Hkv + xn.h / (prm.Hq / prm.Hkv)) * prm.S + (int64_t)kn * L;
+              for (int c = 0; c < D / 64; ++c) {
+                tma_prefetch_l2_2d(&tmK, c * 64, (int32_t)krn);
+                tma_prefetch_l2_2d(&tmV, c * 64, (int32_t)krn);
+              }
+            }
+          }
         }
         // Q tiles: the previous unit's last S products must be done with the Q buffer
         ok = mbar_wait(bar(Ly::B_QEMPTY), (uint32_t)((nq & 1) ^ 1), prm.wait_limit_ns, abort_flag, prm.status,
@@ -492,6 +516,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ++nv;
           }
         }
+        u = un;
       }
       // exit-path drain: every load issued lands before the CTA exits
       if (nq > 0) mbar_drain(bar(Ly::B_QFULL), (uint32_t)((nq - 1) & 1), DRAIN_NS);
