@@ -176,8 +176,20 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(w):
-    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d, "in_dtype": w.dtype,
+def counted_volumes(m, w):
+    """Per-device receive bytes a real mesh (KVR) and a plain ring would move for this workload,
+    counted by the planner (no communication happens on one GPU)."""
+    mesh = m.mesh_attn_plan_create(w.S, w.P, w.causal, w.kvr, w.greedy)
+    _, byts, ring_kv = m.mesh_attn_plan_volumes(mesh, w.Hq, w.Hkv, w.d,
+                                                torch.bfloat16 if w.dtype == "bf16" else torch.float32)
+    per_dev = [sum(b) for b in byts]
+    mx = max(per_dev) if per_dev else 0
+    return {"mesh_max_recv_bytes": mx, "mesh_mean_recv_bytes": sum(per_dev) / max(1, len(per_dev)),
+            "ring_recv_bytes": ring_kv, "reduction_vs_ring": (1 - mx / ring_kv) if ring_kv else None}
+
+
+def workload_config(w, plan="mesh"):
+    return {"workload": w.name, "plan": plan, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d, "in_dtype": w.dtype,
             "causal": w.causal, "P": w.P, "mesh": f"{w.R}x{w.R}", "kvr": w.kvr, "greedy": w.greedy,
             "k_scale": w.k_scale, "l2": "inputs and partials larger than L2 (no flush)"}
 
@@ -189,6 +201,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="bf16_causal_16k", choices=sorted(WORKLOADS))
+    ap.add_argument("--plan", default="mesh", choices=["mesh", "ring"],
+                    help="tile assignment: sqrt(P) x sqrt(P) mesh with KVR (default) or Ring-Attention rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -220,7 +234,10 @@ def main():
 
     q, k, v = make_qkv(w)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    plan = m.mesh_attn_plan_create(w.S, w.P, w.causal, w.kvr, w.greedy)
+    if args.plan == "ring":
+        plan = m.mesh_attn_plan_create_ring(w.S, w.P, w.causal)
+    else:
+        plan = m.mesh_attn_plan_create(w.S, w.P, w.causal, w.kvr, w.greedy)
     po, pl = m.new_partials(plan, w.B, w.Hq, w.d, dev)
     wsp = m.new_workspace(plan, dev)
     st = m.new_status(dev)
@@ -275,7 +292,9 @@ def main():
 
         def e2e_step():
             a, b_, c = qh.to(dev, non_blocking=True), kh.to(dev, non_blocking=True), vh.to(dev, non_blocking=True)
-            Od, Ld = m.mesh_attention(a, b_, c, w.P, w.causal, w.kvr, w.greedy, check_status=False)
+            pe = (m.mesh_attn_plan_create_ring(w.S, w.P, w.causal) if args.plan == "ring"
+                  else m.mesh_attn_plan_create(w.S, w.P, w.causal, w.kvr, w.greedy))
+            Od, Ld = m.mesh_attention(a, b_, c, w.P, w.causal, plan=pe, check_status=False)
             Oh.copy_(Od, non_blocking=True)
             Lh.copy_(Ld, non_blocking=True)
 
@@ -321,13 +340,14 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": workload_config(w),
+        "config": workload_config(w, args.plan),
         "roofline": {"bound": "tensor", "achieved": tile_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": tile_tflops / peaks["bf16_tflops"], "traffic": traffic,
                      "kernel": "tile_fwd_tc_kernel", "peak_kind": f"{peak_kind} bf16 dense burst"},
         "merge": {"bound": "hbm", "achieved": merge_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                   "frac": merge_gbs / peaks["hbm_gbs"], "bytes_per_launch": mbytes, "ms": merge_ms},
         "tile_fwd_ms": tile_ms, "merge_ms": merge_ms,
+        "comm_counted": counted_volumes(m, w),
         "cpu_baseline": cpu_base, "e2e": e2e, "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
     }

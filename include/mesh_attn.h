@@ -73,11 +73,13 @@ typedef struct {
   int64_t S;              /* tokens */
   int64_t L;              /* tokens per partition, S / P */
   int32_t P;              /* partitions = virtual devices = tiles */
-  int32_t R;              /* mesh side, sqrt(P) */
+  int32_t R;              /* mesh side sqrt(P) (0 for a ring plan) */
   int32_t causal, kvr, greedy;
   int32_t n_slots;        /* partial slots = work items, (p, tile) pairs with a live block */
-  int32_t n_steps;        /* greedy steps of the slowest device (0 without greedy) */
-  int32_t reserved;
+  int32_t n_steps;        /* steps of the slowest device (greedy or ring; 0 without greedy) */
+  int32_t layout;         /* 0: sqrt(P) x sqrt(P) mesh tiles; 1: ring rows */
+  int32_t tile_q;         /* Q partitions per tile: R (mesh) or 1 (ring) */
+  int32_t tile_kv;        /* KV partitions per tile: R (mesh) or P (ring) */
   int64_t n_kv_entries;   /* sum over items of their KV partitions = live partition blocks */
   int64_t n_live_blocks;  /* live (p, k) partition blocks of the P x P matrix */
 } mesh_attn_plan_info;
@@ -98,13 +100,22 @@ typedef struct {
 int mesh_attn_plan_create(int64_t S, int32_t P, int32_t causal, int32_t kvr, int32_t greedy,
                           mesh_attn_plan** out);
 
+/* Ring-Attention's work assignment as a plan of the same form, to compare against the mesh
+ * through the same kernels (tutorial §"Ring-Attention 的'阿喀琉斯之踵'" and the 1D ring of
+ * §"Mesh-Attention：从一维'环'到二维'网'", item (a)): device v owns Q partition v and
+ * computes its whole row, visiting KV partitions in ring order v, v-1, ... (own first, one hop
+ * per step); one partial slot per Q partition.  Receive counts: P - 1 KV partitions per device,
+ * no Q and no partial output.  Any P >= 1 (P <= 4096), S >= 0 with S % P == 0. */
+int mesh_attn_plan_create_ring(int64_t S, int32_t P, int32_t causal, mesh_attn_plan** out);
+
 /* Free a plan (NULL is accepted).  The caller must not use it afterwards. */
 int mesh_attn_plan_destroy(mesh_attn_plan* plan);
 
 /* Scalar facts of the plan. */
 int mesh_attn_plan_get_info(const mesh_attn_plan* plan, mesh_attn_plan_info* out);
 
-/* Tile map: q_parts[t*R + j], kv_parts[t*R + k] for t < P (caller arrays of P*R int32). */
+/* Tile map: q_parts[t*tile_q + j], kv_parts[t*tile_kv + k] for t < P (caller arrays of
+ * P*tile_q and P*tile_kv int32; tile_q = tile_kv = R for a mesh plan). */
 int mesh_attn_plan_tiles(const mesh_attn_plan* plan, int32_t* q_parts, int32_t* kv_parts);
 
 /* Partial-slot CSR: slot_off[P + 1] (caller array). */

@@ -166,6 +166,40 @@ def make_plan(S: int, P: int, causal: bool, kvr: bool, greedy: bool) -> Plan:
                 item_step, recv, n_live)
 
 
+def make_ring_plan(S: int, P: int, causal: bool) -> Plan:
+    """Ring-Attention's assignment as a plan of the same shape: device v owns Q partition v and
+    computes its whole row of the Q-KV matrix ("Mesh-Attention" tutorial, the 1D ring of item
+    (a) and the section on Ring-Attention's bottleneck: no Q moves, every KV partition passes
+    through every device).
+
+    Readings: KV partitions reach device v in ring order v, v-1, v-2, ... (its own first, one
+    neighbour hop per step); an item completes at the step its last live block arrives; items are
+    ordered by (step, device); each device receives P-1 KV partitions (a plain ring forwards all
+    of them) and no Q or partial output.
+    """
+    if P < 1:
+        raise ValueError("P must be >= 1")
+    if S < 0 or S % P != 0:
+        raise ValueError("S must be a non-negative multiple of P")
+    L = S // P
+    empty = S == 0
+    q_parts = [[v] for v in range(P)]
+    kv_parts = [[(v - i) % P for i in range(P)] for v in range(P)]
+    slot_off = [0] + [0 if empty else p + 1 for p in range(P)]
+    keyed = []
+    for v in range(P):
+        if empty:
+            continue
+        kvs = [k for k in kv_parts[v] if live(v, k, causal)]
+        done = max(i for i, k in enumerate(kv_parts[v]) if live(v, k, causal))
+        keyed.append(((done, v), (v, v, v), kvs, done))
+    keyed.sort(key=lambda e: e[0])
+    recv = [(0, 0 if empty else P - 1, 0) for _ in range(P)]
+    n_live = 0 if empty else sum(1 for p in range(P) for k in range(P) if live(p, k, causal))
+    return Plan(S, P, 1, L, causal, False, True, q_parts, kv_parts, slot_off, [e[1] for e in keyed],
+                [e[2] for e in keyed], [e[3] for e in keyed], recv, n_live)
+
+
 def ring_recv_partitions(P: int) -> int:
     """KV partitions a device receives in plain Ring-Attention: every other one."""
     return P - 1

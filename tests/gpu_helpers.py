@@ -38,6 +38,7 @@ def check_full(w, O, LSE, q, k, v):
     Or, Lr = OA.attention_bhsd(q, k, v, w.causal)
     to, tl = TOL[w.dtype]
     eo, el = max_err(O, Or), max_err(LSE, Lr)
+    print(f"[parity] {w.name}: max|dO| = {eo:.3e} (tol {to}), max|dLSE| = {el:.3e} (tol {tl})")
     assert eo <= to and el <= tl, f"{w.name}: max|dO| = {eo:.3e} (tol {to}), max|dLSE| = {el:.3e} (tol {tl})"
     return eo, el
 
@@ -76,5 +77,6 @@ def check_sampled(w, O, LSE, q, k, v, rows: np.ndarray):
     Lg = torch.stack([torch.stack([LSE[b, h].cpu()[idx[b, h]] for h in range(w.Hq)]) for b in range(w.B)])
     to, tl = TOL[w.dtype]
     eo, el = max_err(Og, Or), max_err(Lg, Lr)
+    print(f"[parity] {w.name} (sampled rows): max|dO| = {eo:.3e} (tol {to}), max|dLSE| = {el:.3e} (tol {tl})")
     assert eo <= to and el <= tl, f"{w.name}: max|dO| = {eo:.3e} (tol {to}), max|dLSE| = {el:.3e} (tol {tl})"
     return eo, el

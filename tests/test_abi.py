@@ -166,3 +166,30 @@ def test_partials_and_workspace_sizes(lib):
     p = lib.mesh_attn_plan_create(16384, 16, True)
     assert lib.mesh_attn_partials_size(p, 1, 16, 128) == (16 * 58 * 1024 * 128, 16 * 58 * 1024)
     assert lib.mesh_attn_workspace_size(p) >= 17 * 4 + 58 * 16 + 136 * 4
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 7, 16, 100])
+@pytest.mark.parametrize("causal", [0, 1])
+def test_ring_planner_matches_oracle(lib, P, causal):
+    S = P * 5
+    ref = PL.make_ring_plan(S, P, bool(causal))
+    p = lib.mesh_attn_plan_create_ring(S, P, causal)
+    assert p.layout == 1 and p.tile_q == 1 and p.tile_kv == P and p.R == 0
+    q, kv = lib.mesh_attn_plan_tiles(p)
+    assert q == ref.q_parts and kv == ref.kv_parts
+    assert lib.mesh_attn_plan_slots(p) == ref.slot_off
+    items, steps, kvs = lib.mesh_attn_plan_order(p)
+    assert [list(i) for i in items] == [list(i) for i in ref.items]
+    assert steps == ref.item_step and kvs == ref.item_kv
+    counts, _, ring = lib.mesh_attn_plan_volumes(p, 1, 1, 1)
+    assert [list(c) for c in counts] == [list(r) for r in ref.recv]
+
+
+def test_ring_plan_errors(lib):
+    so = lib._lib
+    h = ctypes.c_void_p()
+    assert so.mesh_attn_plan_create_ring(10, 3, 1, ctypes.byref(h)) == 1
+    assert so.mesh_attn_plan_create_ring(12, 0, 1, ctypes.byref(h)) == 1
+    assert so.mesh_attn_plan_create_ring(12, 3, 2, ctypes.byref(h)) == 1
+    p = lib.mesh_attn_plan_create_ring(0, 3, True)
+    assert p.n_slots == 0

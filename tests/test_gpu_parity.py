@@ -96,3 +96,16 @@ def test_full_size_sampled_rows(lib, name):
         g = w.Hq // w.Hkv
         for h in range(w.Hq):
             assert torch.equal(O[0, h, 0].cpu(), v[0, h // g, 0])
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "bf16_L128_causal", "bf16_ragged_L200", "bf16_gqa4_L1024_causal"])
+def test_ring_plan_through_kernels(lib, name):
+    """Ring-Attention's row assignment (one slot per Q partition holding every live KV partition)
+    through the same tile and merge kernels gives the same attention."""
+    w = next(x for x in SMALL if x.name == name)
+    q, k, v = make_qkv(w)
+    plan = lib.mesh_attn_plan_create_ring(w.S, w.P, w.causal)
+    O, LSE, po, pl = lib.mesh_attention(q.cuda(), k.cuda(), v.cuda(), w.P, w.causal, plan=plan, return_partials=True)
+    torch.cuda.synchronize()
+    check_full(w, O, LSE, q, k, v)
+    check_partials(lib, w, plan, po, pl, q, k, v)

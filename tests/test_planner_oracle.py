@@ -176,3 +176,33 @@ def test_empty_sequence_and_bad_args():
     for S, P in [(10, 4), (16, 8), (16, 0), (-4, 4)]:
         with pytest.raises(ValueError):
             PL.make_plan(S, P, True, True, True)
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 7, 16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_plan(P, causal):
+    """Ring-Attention rows: one slot per Q partition covering every live KV partition, visited in
+    ring order (own partition first), P - 1 KV receives per device and nothing else."""
+    p = PL.make_ring_plan(P * 4, P, causal)
+    assert p.slot_off == list(range(P + 1))
+    assert sorted(i[0] for i in p.items) == list(range(P))
+    for (q, t, slot), kvs in zip(p.items, p.item_kv):
+        assert q == t == slot
+        assert kvs[0] == q  # the device's own KV first
+        assert sorted(kvs) == [k for k in range(P) if PL.live(q, k, causal)]
+        assert kvs == [k for k in [(q - i) % P for i in range(P)] if PL.live(q, k, causal)]
+    assert all(r == (0, P - 1, 0) for r in p.recv)
+    assert p.n_live_blocks == (P * (P + 1) // 2 if causal else P * P)
+    steps = p.item_step
+    assert steps == sorted(steps)
+    if causal:  # device v's last live block (KV 0) arrives after v hops
+        assert sorted(steps) == list(range(P))
+
+
+def test_ring_plan_hand_worked():
+    """P = 3 causal, worked by hand: device 2 sees KV 2, 1, 0 (steps 0, 1, 2); device 1 sees KV 1
+    then (ring step 1) KV 0; device 0 only its own KV 0."""
+    p = PL.make_ring_plan(12, 3, True)
+    assert [list(i) for i in p.items] == [[0, 0, 0], [1, 1, 1], [2, 2, 2]]
+    assert p.item_kv == [[0], [1, 0], [2, 1, 0]]
+    assert p.item_step == [0, 1, 2]

@@ -38,12 +38,13 @@ P_sz = ctypes.POINTER(c_sz)
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("S", c_i64), ("L", c_i64), ("P", c_i32), ("R", c_i32), ("causal", c_i32), ("kvr", c_i32),
-                ("greedy", c_i32), ("n_slots", c_i32), ("n_steps", c_i32), ("reserved", c_i32),
-                ("n_kv_entries", c_i64), ("n_live_blocks", c_i64)]
+                ("greedy", c_i32), ("n_slots", c_i32), ("n_steps", c_i32), ("layout", c_i32), ("tile_q", c_i32),
+                ("tile_kv", c_i32), ("n_kv_entries", c_i64), ("n_live_blocks", c_i64)]
 
 
 _SIGS = {
     "mesh_attn_plan_create": (c_i32, [c_i64, c_i32, c_i32, c_i32, c_i32, ctypes.POINTER(c_vp)]),
+    "mesh_attn_plan_create_ring": (c_i32, [c_i64, c_i32, c_i32, ctypes.POINTER(c_vp)]),
     "mesh_attn_plan_destroy": (c_i32, [c_vp]),
     "mesh_attn_plan_get_info": (c_i32, [c_vp, ctypes.POINTER(PlanInfo)]),
     "mesh_attn_plan_tiles": (c_i32, [c_vp, P_i32, P_i32]),
@@ -125,7 +126,7 @@ class Plan:
 
     def __getattr__(self, name):
         if name in ("S", "L", "P", "R", "causal", "kvr", "greedy", "n_slots", "n_steps", "n_kv_entries",
-                    "n_live_blocks"):
+                    "n_live_blocks", "layout", "tile_q", "tile_kv"):
             return getattr(self.__dict__["info"], name)
         raise AttributeError(name)
 
@@ -153,12 +154,18 @@ def mesh_attn_plan_create(S: int, P: int, causal: bool, kvr: bool = True, greedy
     return Plan(h)
 
 
+def mesh_attn_plan_create_ring(S: int, P: int, causal: bool) -> Plan:
+    load_library()
+    h = c_vp()
+    _check(_lib.mesh_attn_plan_create_ring(S, P, int(causal), ctypes.byref(h)), "mesh_attn_plan_create_ring")
+    return Plan(h)
+
+
 def mesh_attn_plan_tiles(plan: Plan):
-    n = plan.P * plan.R
-    q, kv = _i32(n), _i32(n)
+    a, b = plan.tile_q, plan.tile_kv
+    q, kv = _i32(plan.P * a), _i32(plan.P * b)
     _check(_lib.mesh_attn_plan_tiles(plan.handle, q, kv), "mesh_attn_plan_tiles")
-    R = plan.R
-    return ([list(q[t * R:(t + 1) * R]) for t in range(plan.P)], [list(kv[t * R:(t + 1) * R]) for t in range(plan.P)])
+    return ([list(q[t * a:(t + 1) * a]) for t in range(plan.P)], [list(kv[t * b:(t + 1) * b]) for t in range(plan.P)])
 
 
 def mesh_attn_plan_slots(plan: Plan):

@@ -84,6 +84,23 @@ int mesh_attn_plan_create(int64_t S, int32_t P, int32_t causal, int32_t kvr, int
   });
 }
 
+int mesh_attn_plan_create_ring(int64_t S, int32_t P, int32_t causal, mesh_attn_plan** out) {
+  return guarded([&] {
+    if (!out) return fail(MESH_ATTN_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (causal != 0 && causal != 1) return fail(MESH_ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+    mesh_attn_plan* p = new mesh_attn_plan();
+    try {
+      mesh::build_ring_plan(p->p, S, P, causal != 0);
+    } catch (...) {
+      delete p;
+      throw;
+    }
+    *out = p;
+    return (int)MESH_ATTN_OK;
+  });
+}
+
 int mesh_attn_plan_destroy(mesh_attn_plan* plan) {
   delete plan;
   return MESH_ATTN_OK;
@@ -103,6 +120,9 @@ int mesh_attn_plan_get_info(const mesh_attn_plan* plan, mesh_attn_plan_info* out
     out->greedy = p.greedy;
     out->n_slots = p.n_slots();
     out->n_steps = p.n_steps;
+    out->layout = p.layout;
+    out->tile_q = p.tile_q;
+    out->tile_kv = p.tile_kv;
     out->n_kv_entries = (int64_t)p.kv_list.size();
     out->n_live_blocks = p.n_live;
     return (int)MESH_ATTN_OK;

@@ -21,11 +21,13 @@ struct alignas(16) DevItem {
 
 struct Plan {
   int64_t S = 0, L = 0;
-  int32_t P = 0, R = 0;
+  int32_t P = 0, R = 0;          // R: mesh side (0 for a ring plan)
+  int32_t layout = 0;            // 0 mesh, 1 ring
+  int32_t tile_q = 0, tile_kv = 0;  // Q and KV partitions per tile
   bool causal = false, kvr = false, greedy = false;
   int32_t n_steps = 0;
   int64_t n_live = 0;
-  std::vector<int32_t> q_parts, kv_parts;  // [P*R]
+  std::vector<int32_t> q_parts, kv_parts;  // [P*tile_q], [P*tile_kv]
   std::vector<int32_t> slot_off;           // [P+1]
   std::vector<int32_t> items;              // [n*3] (p, t, slot) in execution order
   std::vector<int32_t> item_step;          // [n]
@@ -39,6 +41,7 @@ struct Plan {
 
 // Throws std::invalid_argument / std::bad_alloc; the ABI layer converts.
 void build_plan(Plan& plan, int64_t S, int32_t P, bool causal, bool kvr, bool greedy);
+void build_ring_plan(Plan& plan, int64_t S, int32_t P, bool causal);
 
 // Workspace layout shared by tile_fwd and merge: [slot_off | items | kv_list | counter].
 struct WorkspaceLayout {

@@ -87,6 +87,7 @@ void build_plan(Plan& pl, int64_t S, int32_t P, bool causal, bool kvr, bool gree
   if (S % P != 0) throw std::invalid_argument("S must be a multiple of P");
   pl = Plan();
   pl.S = S; pl.P = P; pl.R = R; pl.L = S / P;
+  pl.layout = 0; pl.tile_q = R; pl.tile_kv = R;
   pl.causal = causal; pl.kvr = kvr; pl.greedy = greedy;
   const bool empty = (S == 0);
 
@@ -185,6 +186,68 @@ void build_plan(Plan& pl, int64_t S, int32_t P, bool causal, bool kvr, bool gree
   }
   pl.kv_off[n] = (int32_t)pos;
   if (pos != pl.n_live) throw std::logic_error("planner: KV entries do not cover the live blocks");
+}
+
+// Ring-Attention's assignment in the same plan form, for comparison through the same kernels:
+// device v owns Q partition v and computes its whole row ("Mesh-Attention" tutorial: the 1D
+// ring, item (a), and the section on Ring-Attention's bottleneck).  KV partitions reach device v
+// in ring order v, v-1, ... (own first, one hop per step); the item completes at the step its
+// last live block arrives; items are ordered by (step, device).  Each device receives P - 1 KV
+// partitions (a plain ring forwards all of them) and no Q or partial output.
+void build_ring_plan(Plan& pl, int64_t S, int32_t P, bool causal) {
+  if (P < 1) throw std::invalid_argument("P must be >= 1");
+  if (P > 4096) throw std::invalid_argument("P must be <= 4096");
+  if (S < 0) throw std::invalid_argument("S must be >= 0");
+  if (S % P != 0) throw std::invalid_argument("S must be a multiple of P");
+  pl = Plan();
+  pl.S = S; pl.P = P; pl.R = 0; pl.L = S / P;
+  pl.layout = 1; pl.tile_q = 1; pl.tile_kv = P;
+  pl.causal = causal; pl.kvr = false; pl.greedy = true;
+  const bool empty = (S == 0);
+  pl.q_parts.resize(P);
+  pl.kv_parts.resize((size_t)P * P);
+  for (int32_t v = 0; v < P; ++v) {
+    pl.q_parts[v] = v;
+    for (int32_t i = 0; i < P; ++i) pl.kv_parts[(size_t)v * P + i] = ((v - i) % P + P) % P;
+  }
+  pl.slot_off.resize(P + 1);
+  for (int32_t p = 0; p <= P; ++p) pl.slot_off[p] = empty ? 0 : p;
+  pl.n_live = empty ? 0 : (causal ? (int64_t)P * (P + 1) / 2 : (int64_t)P * P);
+  pl.recv.assign((size_t)P * 3, 0);
+  if (empty) return;
+  std::vector<std::pair<int32_t, int32_t>> order;  // (completion step, device)
+  order.reserve(P);
+  for (int32_t v = 0; v < P; ++v) {
+    int32_t done = 0;
+    for (int32_t i = 0; i < P; ++i)
+      if (live(v, pl.kv_parts[(size_t)v * P + i], causal)) done = i;
+    order.push_back({done, v});
+    pl.recv[(size_t)v * 3 + 1] = P - 1;
+  }
+  std::stable_sort(order.begin(), order.end());
+  pl.items.resize((size_t)P * 3);
+  pl.item_step.resize(P);
+  pl.kv_off.resize((size_t)P + 1);
+  pl.dev_items.resize(P);
+  int64_t pos = 0;
+  for (int32_t i = 0; i < P; ++i) {
+    const int32_t v = order[i].second;
+    pl.items[(size_t)i * 3 + 0] = v;
+    pl.items[(size_t)i * 3 + 1] = v;
+    pl.items[(size_t)i * 3 + 2] = v;
+    pl.item_step[i] = order[i].first;
+    pl.kv_off[i] = (int32_t)pos;
+    int32_t n = 0;
+    for (int32_t j = 0; j < P; ++j) {
+      const int32_t k = pl.kv_parts[(size_t)v * P + j];
+      if (live(v, k, causal)) { pl.kv_list.push_back(k); ++n; }
+    }
+    pl.dev_items[i] = DevItem{v, v, (int32_t)pos, n};
+    pos += n;
+    pl.n_steps = std::max(pl.n_steps, order[i].first);
+  }
+  pl.kv_off[P] = (int32_t)pos;
+  if (pos != pl.n_live) throw std::logic_error("ring planner: KV entries do not cover the live blocks");
 }
 
 WorkspaceLayout workspace_layout(const Plan& pl) {
