@@ -27,6 +27,12 @@ SMALL = [
     Workload(107, "f32_ragged_L100_causal", 1, 2, 1, 900, 128, "f32", True, 9),
     Workload(108, "bf16_peaked_k4", 1, 2, 1, 4096, 128, "bf16", True, 16, k_scale=4.0),
     Workload(109, "bf16_single_partition", 1, 1, 1, 640, 128, "bf16", True, 1),
+    Workload(111, "bf16_one_token_partitions", 1, 2, 1, 16, 128, "bf16", True, 16),
+    Workload(112, "bf16_tiny_partitions_L8", 1, 2, 2, 512, 128, "bf16", True, 64),
+    Workload(113, "bf16_batch2_gqa_ragged_causal", 2, 4, 2, 800, 128, "bf16", True, 4),
+    Workload(114, "bf16_mqa_32_heads", 1, 32, 1, 1024, 128, "bf16", True, 4),
+    Workload(115, "f32_gqa_d64", 1, 4, 2, 765, 64, "f32", False, 9),
+    Workload(116, "bf16_noncausal_d64_L1000", 1, 2, 1, 4000, 64, "bf16", False, 4),
 ]
 
 
