@@ -68,6 +68,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int64_t
   }
 }
 
+// mbar_wait for a whole converged warp: every lane polls and the result is warp-uniform, so the
+// warp stays converged after the wait.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, int64_t limit_ns,
+                                               volatile int32_t* abort, int32_t* status, int32_t role,
+                                               int32_t unit) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    if (__any_sync(0xffffffffu, *abort != 0)) return false;
+    if (__any_sync(0xffffffffu, (int64_t)(global_timer_ns() - t0) > limit_ns)) {
+      if ((threadIdx.x & 31) == 0) {
+        *abort = 1;
+        record_error(status, MESH_ATTN_ERR_DEVICE_TIMEOUT, role, unit);
+      }
+      __syncwarp();
+      return false;
+    }
+  }
+}
+
 // Drain wait: used on the exit path only, with its own fixed limit and no abort check.
 __device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, int64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
@@ -137,6 +158,39 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+
+// Warp-converged forms: the whole warp executes the call with warp-uniform operands and one lane,
+// chosen by elect.sync inside the same instruction sequence, issues.  Keeping the issuing warp
+// converged lets the operands live in uniform registers, which makes an issue several times
+// cheaper for the issuing warp than a lane-0-only branch; at M = N = 128, K = 16 an MMA runs for
+// 64 cycles, so the issue cost decides whether one warp keeps the tensor pipe fed.
+__device__ __forceinline__ void tc_mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
 }
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }

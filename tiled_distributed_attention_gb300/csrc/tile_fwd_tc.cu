@@ -15,7 +15,7 @@
 //               planned order, item-major), publishes it through a 2-slot ring in shared
 //               memory, then TMA-loads the unit's two Q tiles and streams K and V blocks
 //               (128 rows x 64 columns, 128-byte swizzle) through a 2-stage mbarrier ring.
-//   warp 8      MMA issuer (one thread): S_t = Q_t K^T and O_t += P_t V with
+//   warp 8      MMA issuer (one elected lane of a converged warp): S_t = Q_t K^T and O_t += P_t V with
 //               tcgen05.mma.cta_group::1.kind::f16 (M = N = 128, K = 16), fp32 accumulators in
 //               tensor memory, completion signalled with tcgen05.commit.
 //   warps 0-7   softmax, one warpgroup per query tile; thread i owns row i (TMEM lane i), so
@@ -46,8 +46,8 @@ constexpr int BM = 128;  // query rows per tile = TMEM lanes
 constexpr int BN = 128;  // keys per KV block
 constexpr int NST = 2;   // K/V ring stages
 constexpr int NUM_THREADS = 384;
-constexpr int SOFTMAX_REGS = 200;  // 2 x 128 x 200 + 128 x 96 <= 384 x 168 registers at launch
-constexpr int OTHER_REGS = 96;
+constexpr int SOFTMAX_REGS = 200;  // 2 x 128 x 200 + 128 x 104 <= 384 x 168 registers at launch
+constexpr int OTHER_REGS = 104;
 constexpr int WARP_MMA = 8;
 constexpr int WARP_LOAD = 9;
 constexpr float LOG2_RESCALE = 8.0f;
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(Ly::B_OFINAL + t), 1);
       mbar_init(bar(Ly::B_OFREE + t), BM);
       mbar_init(bar(Ly::B_UFULL + t), 1);
-      mbar_init(bar(Ly::B_UEMPTY + t), 1 + 8);  // MMA thread + one lane of each softmax warp
+      mbar_init(bar(Ly::B_UEMPTY + t), 1 + 8);  // one lane of the MMA warp and of each softmax warp
     }
     mbar_init(bar(Ly::B_DRAIN), 1);
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0) ? 1 : 0;
@@ -328,15 +328,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     regs_dec<OTHER_REGS>();
-    if (warp == WARP_MMA && lane == 0) {
+    if (warp == WARP_MMA) {
       // ================================================================ MMA issuer
+      // The whole warp runs this loop converged; tcgen05.mma and tcgen05.commit are issued by
+      // one elected lane (tc_*_warp), every wait is warp-uniform (mbar_wait_warp).
       constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
       // Base descriptors are built once; per instruction only the start-address field (the
       // low 14 bits, address / 16) advances by a compile-time offset.  Shared addresses stay
       // below 256 KB, so the addition never carries out of that field.  Keeping the issuing
-      // thread's work per MMA to a few independent adds is what lets one thread keep the
-      // tensor pipe fed.
+      // warp's work per MMA to a few independent adds on uniform values is what lets one warp
+      // keep the tensor pipe fed.
       const uint64_t q_desc0 = smem_desc_sw128(sb + Ly::Q_OFF, 16u, 1024u);
       const uint64_t k_desc0 = smem_desc_sw128(sb + Ly::K_OFF, 16u, 1024u);
       const uint64_t v_desc0 = smem_desc_sw128(sb + Ly::V_OFF, Ly::BOX, 1024u);
@@ -350,8 +352,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint64_t kd = k_desc0 + (uint64_t)stage * TILE16;
         const uint32_t d_tm = tmem + (uint32_t)(t * 128);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) tc_mma_ss(d_tm, qd + kmaj_off(kk), kd + kmaj_off(kk), idesc_qk, kk > 0);
-        tc_commit(bar(Ly::B_SFULL + t));
+        for (int kk = 0; kk < D / 16; ++kk) tc_mma_ss_warp(d_tm, qd + kmaj_off(kk), kd + kmaj_off(kk), idesc_qk, kk > 0);
+        tc_commit_warp(bar(Ly::B_SFULL + t));
       };
       auto issue_pv = [&](int t, int stage, bool first) {
         const uint64_t vd = v_desc0 + (uint64_t)stage * TILE16;
@@ -359,18 +361,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t tm_o = tmem + 256u + (uint32_t)(t * 128);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          tc_mma_ts(tm_o, tm_p + (uint32_t)(kk * 8), vd + (uint64_t)(kk * 128), idesc_pv, (!first || kk > 0) ? 1u : 0u);
+          tc_mma_ts_warp(tm_o, tm_p + (uint32_t)(kk * 8), vd + (uint64_t)(kk * 128), idesc_pv, (!first || kk > 0) ? 1u : 0u);
       };
       int nu = 0, nblk = 0;
       int cnt[2] = {0, 0}, uses[2] = {0, 0};
       bool ok = true;
       while (ok) {
         const int slot = nu & 1;
-        ok = mbar_wait(bar(Ly::B_UFULL + slot), (uint32_t)((nu >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+        ok = mbar_wait_warp(bar(Ly::B_UFULL + slot), (uint32_t)((nu >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
                        ROLE_MMA, -1);
         if (!ok) break;
         const int u = unit_ring[slot];
-        mbar_arrive(bar(Ly::B_UEMPTY + slot));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(Ly::B_UEMPTY + slot));
+        __syncwarp();
         const int uidx = nu++;
         if (u < 0) break;
         const Unit x = decode(u, prm);
@@ -378,38 +382,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int32_t* kvl = prm.kv_list + x.it.kv_off;
         int NB = 0;
         for (int ki = 0; ki < x.it.n_kv; ++ki) NB += blocks_of(__ldg(kvl + ki), x.it.p, prm.causal, x.nb, x.a_max);
-        ok = mbar_wait(bar(Ly::B_QFULL), (uint32_t)(uidx & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, u);
+        ok = mbar_wait_warp(bar(Ly::B_QFULL), (uint32_t)(uidx & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, u);
         if (ok)
-          ok = mbar_wait(bar(Ly::B_KFULL + nblk % NST), (uint32_t)((nblk / NST) & 1), prm.wait_limit_ns, abort_flag,
+          ok = mbar_wait_warp(bar(Ly::B_KFULL + nblk % NST), (uint32_t)((nblk / NST) & 1), prm.wait_limit_ns, abort_flag,
                          prm.status, ROLE_MMA, u);
         if (!ok) break;
         tc_fence_after();
         for (int t = 0; t < x.ntiles; ++t) issue_s(t, nblk % NST);
-        if (NB == 1) tc_commit(bar(Ly::B_QEMPTY));
-        tc_commit(bar(Ly::B_KEMPTY + nblk % NST));
+        if (NB == 1) tc_commit_warp(bar(Ly::B_QEMPTY));
+        tc_commit_warp(bar(Ly::B_KEMPTY + nblk % NST));
         for (int j = 0; j < NB && ok; ++j) {
           const int g = nblk + j;
           const int st = g % NST;
-          ok = mbar_wait(bar(Ly::B_VFULL + st), (uint32_t)((g / NST) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+          ok = mbar_wait_warp(bar(Ly::B_VFULL + st), (uint32_t)((g / NST) & 1), prm.wait_limit_ns, abort_flag, prm.status,
                          ROLE_MMA, u);
           for (int t = 0; t < x.ntiles && ok; ++t) {
-            ok = mbar_wait(bar(Ly::B_PFULL + t), (uint32_t)(cnt[t] & 1), prm.wait_limit_ns, abort_flag, prm.status,
+            ok = mbar_wait_warp(bar(Ly::B_PFULL + t), (uint32_t)(cnt[t] & 1), prm.wait_limit_ns, abort_flag, prm.status,
                            ROLE_MMA, u);
             if (ok && j == 0 && uses[t] > 0)  // the previous unit's epilogue has copied O_t out
-              ok = mbar_wait(bar(Ly::B_OFREE + t), (uint32_t)((uses[t] - 1) & 1), prm.wait_limit_ns, abort_flag,
+              ok = mbar_wait_warp(bar(Ly::B_OFREE + t), (uint32_t)((uses[t] - 1) & 1), prm.wait_limit_ns, abort_flag,
                              prm.status, ROLE_MMA, u);
             if (!ok) break;
             tc_fence_after();
             issue_pv(t, st, j == 0);
             ++cnt[t];
             if (j + 1 == NB) {  // tile t's last product of the unit: its epilogue may start
-              tc_commit(bar(Ly::B_OFINAL + t));
+              tc_commit_warp(bar(Ly::B_OFINAL + t));
               ++uses[t];
             }
             if (j + 1 < NB) {
               const int sn = (g + 1) % NST;
               if (t == 0) {
-                ok = mbar_wait(bar(Ly::B_KFULL + sn), (uint32_t)(((g + 1) / NST) & 1), prm.wait_limit_ns, abort_flag,
+                ok = mbar_wait_warp(bar(Ly::B_KFULL + sn), (uint32_t)(((g + 1) / NST) & 1), prm.wait_limit_ns, abort_flag,
                                prm.status, ROLE_MMA, u);
                 if (!ok) break;
                 tc_fence_after();
@@ -418,15 +422,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           if (!ok) break;
-          if (j + 1 < NB) tc_commit(bar(Ly::B_KEMPTY + (g + 1) % NST));
-          if (j + 2 == NB) tc_commit(bar(Ly::B_QEMPTY));  // the unit's last S products are issued
-          tc_commit(bar(Ly::B_VEMPTY + st));
+          if (j + 1 < NB) tc_commit_warp(bar(Ly::B_KEMPTY + (g + 1) % NST));
+          if (j + 2 == NB) tc_commit_warp(bar(Ly::B_QEMPTY));  // the unit's last S products are issued
+          tc_commit_warp(bar(Ly::B_VEMPTY + st));
         }
         if (!ok) break;
         nblk += NB;
       }
       // exit-path drain: every MMA issued completes before TMEM is freed
-      tc_commit(bar(Ly::B_DRAIN));
+      tc_commit_warp(bar(Ly::B_DRAIN));
       mbar_drain(bar(Ly::B_DRAIN), 0u, DRAIN_NS);
     } else if (warp == WARP_LOAD && lane == 0) {
       // ================================================================ producer
