@@ -51,6 +51,9 @@ constexpr int OTHER_REGS = 104;
 constexpr int WARP_MMA = 8;
 constexpr int WARP_LOAD = 9;
 constexpr float LOG2_RESCALE = 8.0f;
+// Row sum of one block accepted without a max pass: every term is then at most 2^16, and a sum
+// this large implies a row maximum more than 2^LOG2_RESCALE above the reference (2^16 / BN > 2^8).
+constexpr float SUM_ACCEPT = 65536.0f;
 constexpr int64_t DRAIN_NS = 200000000;  // exit-path waits for copies in flight
 
 // roles recorded with an error
@@ -215,38 +218,73 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
-          float s[BN];
-#pragma unroll
-          for (int c = 0; c < BN; c += 32) tmem_ld32(tm_s + (uint32_t)c, s + c);
-          tc_wait_ld();
           // mask: causal diagonal block (key column > query row) and keys past the partition
           const int kv_valid = (int)min((int64_t)BN, L - (int64_t)jb * BN);
           int lim = BN - 1;
           if (diag) lim = (jb < a_t) ? BN - 1 : (jb == a_t ? row : -1);
           lim = min(lim, kv_valid - 1);
-          if (lim < BN - 1) {
+          // The exponentials use the row's running reference m_used, which only ever grows.  A
+          // block whose row maximum stays within 2^LOG2_RESCALE of it needs no maximum at all, so
+          // the common case skips the max pass: exponentiate against m_used and accept the block
+          // when its row sum is at most SUM_ACCEPT (every term is then bounded as well).  A row
+          // without a reference yet (first block of the unit), or a block whose sum is too large
+          // or not finite, takes the row maximum first, raising m_used (and rescaling O and l)
+          // when it grew by more than 2^LOG2_RESCALE, and the exponentials are redone.
+          bool need_max = __any_sync(0xffffffffu, m_used == -INFINITY);
+          float factor = 1.f, blk = 0.f;
+          uint32_t pk[BN / 2];
+#pragma unroll 1
+          for (int pass = 0;; ++pass) {
+            // S_t stays in TMEM until P_t is written, so a second pass reloads it rather than
+            // keeping 128 scores live across the pass
+            float s[BN];
 #pragma unroll
-            for (int c = 0; c < BN; ++c)
-              if (c > lim) s[c] = -INFINITY;
-          }
-          // row max: four independent chains of 3-input max
-          float mc[4];
+            for (int c = 0; c < BN; c += 32) tmem_ld32(tm_s + (uint32_t)c, s + c);
+            tc_wait_ld();
+            if (lim < BN - 1) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float v = max3f(s[32 * q], s[32 * q + 1], s[32 * q + 2]);
-#pragma unroll
-            for (int i = 3; i + 1 < 32; i += 2) v = max3f(v, s[32 * q + i], s[32 * q + i + 1]);
-            mc[q] = fmaxf(v, s[32 * q + 31]);
-          }
-          const float m_new = fmaxf(max3f(mc[0], mc[1], mc[2]), mc[3]) * prm.scale_log2;
-          float factor = 1.f;
-          if (m_new > -INFINITY) {
-            if (m_used == -INFINITY) {
-              m_used = m_new;
-            } else if (m_new > m_used + LOG2_RESCALE) {
-              factor = fast_exp2(m_used - m_new);
-              m_used = m_new;
+              for (int c = 0; c < BN; ++c)
+                if (c > lim) s[c] = -INFINITY;
             }
+            if (need_max) {
+              // row max: four independent chains of 3-input max
+              float mc[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                float v = max3f(s[32 * q], s[32 * q + 1], s[32 * q + 2]);
+#pragma unroll
+                for (int i = 3; i + 1 < 32; i += 2) v = max3f(v, s[32 * q + i], s[32 * q + i + 1]);
+                mc[q] = fmaxf(v, s[32 * q + 31]);
+              }
+              const float m_new = fmaxf(max3f(mc[0], mc[1], mc[2]), mc[3]) * prm.scale_log2;
+              if (m_new > -INFINITY) {
+                if (m_used == -INFINITY) {
+                  m_used = m_new;
+                } else if (m_new > m_used + LOG2_RESCALE) {
+                  factor *= fast_exp2(m_used - m_new);
+                  m_used = m_new;
+                }
+              }
+            }
+            const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+            // p = 2^(s * scale * log2 e - m): two elements per FMA, four independent sum chains
+            const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2);
+            const uint64_t nm2 = f2_pack(-mref, -mref);
+            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+            for (int c = 0; c < BN / 2; ++c) {
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sc2, nm2), x0, x1);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              acc2[c & 3] = f2_add(acc2[c & 3], f2_pack(p0, p1));
+              pk[c] = pack_bf16x2(p0, p1);
+            }
+            float sa, sb2;
+            f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), sa, sb2);
+            blk = sa + sb2;
+            // NaN fails the comparison: a NaN row takes the max pass once and is then accepted
+            if (pass == 1 || __all_sync(0xffffffffu, blk <= SUM_ACCEPT)) break;
+            need_max = true;
           }
           if (__any_sync(0xffffffffu, factor != 1.f)) {
             // O_t holds every earlier PV product of this unit: S_t(j) was issued after
@@ -263,23 +301,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tmem_st32(tm_o + (uint32_t)c, w);
             }
           }
-          const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-          // p = 2^(s * scale * log2 e - m): two elements per FMA, four independent sum chains
-          const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2);
-          const uint64_t nm2 = f2_pack(-mref, -mref);
-          uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-          uint32_t pk[BN / 2];
-#pragma unroll
-          for (int c = 0; c < BN / 2; ++c) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sc2, nm2), x0, x1);
-            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            acc2[c & 3] = f2_add(acc2[c & 3], f2_pack(p0, p1));
-            pk[c] = pack_bf16x2(p0, p1);
-          }
-          float sa, sb2;
-          f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), sa, sb2);
-          l_sum += sa + sb2;
+          l_sum += blk;
           tmem_st32(tm_s, pk);
           tmem_st32(tm_s + 32u, pk + 32);
           tc_wait_st();
