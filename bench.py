@@ -379,9 +379,11 @@ def main():
         import hashlib
         with open(prof) as f:
             rec = json.load(f).get(w.name, {}).get("tile_fwd")
-        src = os.path.join(ROOT, "tiled_distributed_attention_gb300", "csrc", "tile_fwd_tc.cu")
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        h = hashlib.sha256()
+        for name in ("tile_fwd_tc.cu", "ptx.cuh"):  # the kernel and the inline-PTX helpers it uses
+            with open(os.path.join(ROOT, "tiled_distributed_attention_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        sha = h.hexdigest()
         # counters only describe the kernel they were taken on
         if rec and sha.startswith(rec["source_sha256_prefix"]):
             traffic = rec["bytes"]
