@@ -216,3 +216,36 @@ def volume_bytes(plan: Plan, Hq: int, Hkv: int, d: int, elem_bytes: int):
     ob = plan.L * Hq * (4 * d + 4)
     per = [(q * qb, kv * kvb, o * ob) for (q, kv, o) in plan.recv]
     return per, ring_recv_partitions(plan.P) * kvb
+
+
+@dataclasses.dataclass
+class KvSlots:
+    """Backward pass: the partial dK / dV slots of a plan."""
+    kv_slot_off: List[int]  # [P+1]: the slots of KV partition k are kv_slot_off[k] .. kv_slot_off[k+1]-1
+    kv_items: List[Tuple[int, int, int]]  # (k, t, kv_slot) in slot order
+    kv_item_q: List[List[int]]  # the tile's Q partitions with a live block for k, ascending
+
+
+def kv_slots(plan: Plan) -> KvSlots:
+    """The (KV partition k, tile t) pairs of a plan that hold at least one live block.
+
+    In the backward pass tile t sums dK and dV of each of its KV partitions over its own Q
+    partitions; those partial sums go back along the mesh column to k's owner, as the forward's
+    partial outputs go back along the mesh row to the Q owner.  Readings: slots are grouped by k,
+    tiles ascending within a group, and the backward visits them in slot order.
+    """
+    P = plan.P
+    off = [0]
+    items: List[Tuple[int, int, int]] = []
+    item_q: List[List[int]] = []
+    empty = plan.S == 0
+    for k in range(P):
+        for t in range(len(plan.q_parts)):
+            if empty or k not in plan.kv_parts[t]:
+                continue
+            qs = sorted(p for p in plan.q_parts[t] if live(p, k, plan.causal))
+            if qs:
+                items.append((k, t, len(items)))
+                item_q.append(qs)
+        off.append(len(items))
+    return KvSlots(off, items, item_q)
