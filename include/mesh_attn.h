@@ -82,6 +82,8 @@ typedef struct {
   int32_t tile_kv;        /* KV partitions per tile: R (mesh) or P (ring) */
   int64_t n_kv_entries;   /* sum over items of their KV partitions = live partition blocks */
   int64_t n_live_blocks;  /* live (p, k) partition blocks of the P x P matrix */
+  int32_t n_kv_slots;     /* backward: (KV partition, tile) pairs with a live block */
+  int32_t reserved;
 } mesh_attn_plan_info;
 
 /* Build the tile plan (tutorial §"Mesh-Attention：从一维'环'到二维'网'", items (b) and (c);
@@ -205,6 +207,69 @@ int mesh_attn_merge(const mesh_attn_plan* plan, mesh_attn_dtype out_dtype, int32
                     int32_t Hq, int32_t d, const float* partial_o, const float* partial_lse,
                     void* O, float* LSE, void* workspace, size_t workspace_bytes,
                     int32_t* d_status, void* stream);
+
+/* ---------------------------------------------------------------- backward pass
+ *
+ * The pages describe the forward pass; Mesh-Attention is a training method (tutorial: end-to-end
+ * training speedups; closing remarks on large-model training), so the backward pass keeps the
+ * forward's tile structure.  With the forward's global LSE and an upstream gradient dO:
+ *   P_ij = exp(scale q_i.k_j - LSE_i) over the visible keys,  dP_ij = dO_i . v_j,
+ *   D_i = dO_i . O_i,  dS_ij = P_ij (dP_ij - D_i),
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,  dV_j = sum_i P_ij dO_i,
+ * a KV head's dK and dV summing over its query heads.  Tile t computes, for each of its work
+ * items (p, t), the dQ sums over its KV partitions into the item's partial slot (the forward's
+ * slots: summed along the mesh row), and for each of its KV partitions k with a live block, the
+ * dK / dV sums over its Q partitions into a KV slot (summed along the mesh column back to k's
+ * owner).  Partials are fp32:
+ *   dq_partial [B, Hq, n_slots, L, d];  dk_partial, dv_partial [B, Hkv, n_kv_slots, L, d].
+ * Call order: mesh_attn_bwd_prep (D), mesh_attn_tile_bwd, mesh_attn_bwd_reduce. */
+
+/* KV slots: kv_slot_off[P + 1] (the slots of KV partition k are kv_slot_off[k] ..
+ * kv_slot_off[k+1] - 1, grouped by k, tiles ascending); kv_items[3 i + 0..2] = (k, tile t,
+ * kv slot i); the tile's Q partitions with a live block for k, ascending, are
+ * q_list[q_off[i] .. q_off[i+1]).  Caller arrays of P + 1, n_kv_slots * 3, n_kv_slots + 1 and
+ * n_live_blocks int32; any may be NULL to skip it. */
+int mesh_attn_plan_kv_slots(const mesh_attn_plan* plan, int32_t* kv_slot_off, int32_t* kv_items,
+                            int32_t* q_off, int32_t* q_list);
+
+/* Element counts of the backward partials: *dq_elems = B*Hq*n_slots*L*d for dq_partial,
+ * *dkv_elems = B*Hkv*n_kv_slots*L*d for each of dk_partial and dv_partial. */
+int mesh_attn_bwd_partials_size(const mesh_attn_plan* plan, int32_t B, int32_t Hq, int32_t Hkv,
+                                int32_t d, size_t* dq_elems, size_t* dkv_elems);
+
+/* Bytes of device workspace mesh_attn_tile_bwd and mesh_attn_bwd_reduce need (both work lists,
+ * both slot CSRs, two scheduling counters); caller-allocated, 16-byte aligned, reusable across
+ * calls on one stream. */
+int mesh_attn_bwd_workspace_size(const mesh_attn_plan* plan, size_t* bytes);
+
+/* D[b, h, i] = sum_e dO[b, h, i, e] * O[b, h, i, e] in fp32 (the row term of dS).
+ *   dtype of O and dO: MESH_ATTN_BF16 or MESH_ATTN_F32; O, dO [B, Hq, S, d] 16-byte aligned;
+ *   D [B, Hq, S] fp32; d 64 or 128. */
+int mesh_attn_bwd_prep(mesh_attn_dtype dtype, int32_t B, int32_t Hq, int64_t S, int32_t d,
+                       const void* O, const void* dO, float* D, int32_t* d_status, void* stream);
+
+/* Tile attention backward: the partial gradients above for every batch and head.
+ *   in_dtype  MESH_ATTN_BF16 (tensor-core kernels: bf16 products with fp32 accumulation; P and
+ *             dS rounded to bf16 for the products that take them) or MESH_ATTN_F32 (CUDA-core
+ *             kernels, fp32 throughout).
+ *   Q, K, V, dO of in_dtype (dO [B, Hq, S, d]), 16-byte aligned; LSE [B, Hq, S] fp32 as written by
+ *   mesh_attn_merge; D from mesh_attn_bwd_prep; scale as in the forward call.
+ *   dq_partial, dk_partial, dv_partial: fp32 outputs, sizes from mesh_attn_bwd_partials_size.
+ *   Other arguments as for mesh_attn_tile_fwd.  Rows with LSE = -inf contribute nothing. */
+int mesh_attn_tile_bwd(const mesh_attn_plan* plan, mesh_attn_dtype in_dtype, int32_t B, int32_t Hq,
+                       int32_t Hkv, int32_t d, const void* Q, const void* K, const void* V,
+                       const void* dO, const float* LSE, const float* D, float scale,
+                       float* dq_partial, float* dk_partial, float* dv_partial, void* workspace,
+                       size_t workspace_bytes, int32_t* d_status, void* stream);
+
+/* Sum the backward partials: dQ [B, Hq, S, d] over the slots of each Q partition, dK and dV
+ * [B, Hkv, S, d] over the KV slots of each KV partition, rounded to out_dtype (nearest even for
+ * bf16).  Outputs 16-byte aligned; other arguments as for mesh_attn_merge. */
+int mesh_attn_bwd_reduce(const mesh_attn_plan* plan, mesh_attn_dtype out_dtype, int32_t B,
+                         int32_t Hq, int32_t Hkv, int32_t d, const float* dq_partial,
+                         const float* dk_partial, const float* dv_partial, void* dQ, void* dK,
+                         void* dV, void* workspace, size_t workspace_bytes, int32_t* d_status,
+                         void* stream);
 
 /* Synchronise `stream`, copy word 0 of the device status block to *out (a mesh_attn_status).
  * Returns MESH_ATTN_ERR_CUDA if the copy or the synchronisation failed. */

@@ -9,9 +9,9 @@ A New Communication-Efficient Distributed Attention with Improved Data Locality"
 abstract: 1M-token sequences on clusters; no dataset is named), restated as five
 single-GPU configurations.  Inputs are i.i.d. N(0, 1) draws from NumPy's PCG64,
 seeded with ``SeedSequence([20251224, cfg_id, tensor_id])`` where tensor_id is
-Q=0, K=1, V=2 and the sampled-row stream is 3.  bf16 inputs are the float32 draw
-rounded to nearest even.  The stress workload multiplies K by 4 after rounding,
-which is exact in bf16 (a power of two).
+Q=0, K=1, V=2, the sampled-row stream 3 and the backward pass's upstream gradient
+dO 4.  bf16 inputs are the float32 draw rounded to nearest even.  The stress workload
+multiplies K by 4 after rounding, which is exact in bf16 (a power of two).
 """
 from __future__ import annotations
 
@@ -22,7 +22,7 @@ import numpy as np
 import torch
 
 SEED_ROOT = 20251224
-TENSOR_Q, TENSOR_K, TENSOR_V, TENSOR_ROWS = 0, 1, 2, 3
+TENSOR_Q, TENSOR_K, TENSOR_V, TENSOR_ROWS, TENSOR_DO = 0, 1, 2, 3, 4
 
 
 @dataclasses.dataclass(frozen=True)
@@ -105,6 +105,12 @@ def make_qkv(w: Workload, seed_offset: int = 0):
     k = normal_tensor(cid, TENSOR_K, (w.B, w.Hkv, w.S, w.d), w.dtype, scale=w.k_scale)
     v = normal_tensor(cid, TENSOR_V, (w.B, w.Hkv, w.S, w.d), w.dtype)
     return q, k, v
+
+
+def make_do(w: Workload, seed_offset: int = 0) -> torch.Tensor:
+    """The upstream gradient dO [B,Hq,S,d] of the backward pass: N(0,1) in the workload's dtype."""
+    cid = w.cfg_id + 1000 * seed_offset
+    return normal_tensor(cid, TENSOR_DO, (w.B, w.Hq, w.S, w.d), w.dtype)
 
 
 def forced_rows(S: int, P: int) -> List[int]:

@@ -193,3 +193,67 @@ def test_ring_plan_errors(lib):
     assert so.mesh_attn_plan_create_ring(12, 3, 2, ctypes.byref(h)) == 1
     p = lib.mesh_attn_plan_create_ring(0, 3, True)
     assert p.n_slots == 0
+
+
+@pytest.mark.parametrize("P", [1, 4, 9, 16, 64])
+@pytest.mark.parametrize("causal,kvr", list(itertools.product([0, 1], repeat=2)))
+def test_kv_slots_match_oracle(lib, P, causal, kvr):
+    """Backward KV slots of the C++ planner equal the plain-Python planner's, bit for bit."""
+    S = P * 3
+    ref = PL.kv_slots(PL.make_plan(S, P, bool(causal), bool(kvr), True))
+    p = lib.mesh_attn_plan_create(S, P, causal, kvr, True)
+    off, items, qs = lib.mesh_attn_plan_kv_slots(p)
+    assert p.n_kv_slots == len(ref.kv_items)
+    assert off == ref.kv_slot_off
+    assert [list(i) for i in items] == [list(i) for i in ref.kv_items]
+    assert qs == ref.kv_item_q
+
+
+@pytest.mark.parametrize("P", [1, 3, 7])
+def test_kv_slots_ring_match_oracle(lib, P):
+    for causal in (0, 1):
+        ref = PL.kv_slots(PL.make_ring_plan(P * 2, P, bool(causal)))
+        p = lib.mesh_attn_plan_create_ring(P * 2, P, causal)
+        off, items, qs = lib.mesh_attn_plan_kv_slots(p)
+        assert off == ref.kv_slot_off and [list(i) for i in items] == [list(i) for i in ref.kv_items]
+        assert qs == ref.kv_item_q
+
+
+def test_backward_sizes_and_status_codes(lib):
+    so = lib._lib
+    p = lib.mesh_attn_plan_create(16384, 16, True)
+    assert p.n_kv_slots == 40  # R^2 (R + 1) / 2 for R = 4
+    assert lib.mesh_attn_bwd_partials_size(p, 1, 16, 4, 128) == (16 * 58 * 1024 * 128, 4 * 40 * 1024 * 128)
+    ws = lib.mesh_attn_bwd_workspace_size(p)
+    assert ws >= 17 * 4 + 58 * 16 + 136 * 4 + 17 * 4 + 40 * 16 + 136 * 4 + 512
+    fake = ctypes.c_void_p(1 << 20)
+
+    def tile(**kw):
+        a = dict(plan=p.handle, dt=1, B=1, Hq=2, Hkv=1, d=128, scale=0.1, wsb=ws, dO=fake)
+        a.update(kw)
+        return so.mesh_attn_tile_bwd(a["plan"], a["dt"], a["B"], a["Hq"], a["Hkv"], a["d"], fake, fake, fake, a["dO"],
+                                     fake, fake, a["scale"], fake, fake, fake, fake, a["wsb"], fake, None)
+
+    assert tile(plan=None) == 1
+    assert tile(d=96) == 2
+    assert tile(Hkv=3) == 1
+    assert tile(dt=7) == 1
+    assert tile(scale=-1.0) == 1
+    assert tile(dO=None) == 1
+    assert tile(dO=ctypes.c_void_p((1 << 20) + 4)) == 3
+    assert tile(wsb=ws - 1) == 9
+    assert tile(B=0) == 0 and tile(Hq=0) == 0
+    assert so.mesh_attn_bwd_prep(1, 1, 2, 1024, 100, fake, fake, fake, fake, None) == 2
+    assert so.mesh_attn_bwd_prep(5, 1, 2, 1024, 128, fake, fake, fake, fake, None) == 1
+    assert so.mesh_attn_bwd_prep(1, 0, 2, 1024, 128, None, None, None, None, None) == 0
+    assert so.mesh_attn_bwd_reduce(p.handle, 1, 1, 2, 1, 128, fake, fake, fake, fake, fake, fake, fake, ws - 1, fake,
+                                   None) == 9
+    assert so.mesh_attn_bwd_reduce(p.handle, 1, 1, 2, 3, 128, fake, fake, fake, fake, fake, fake, fake, ws, fake,
+                                   None) == 1
+    empty = lib.mesh_attn_plan_create(0, 16, True)
+    assert empty.n_kv_slots == 0
+    assert lib.mesh_attn_bwd_partials_size(empty, 2, 4, 2, 128) == (0, 0)
+    assert so.mesh_attn_tile_bwd(empty.handle, 1, 1, 2, 1, 128, None, None, None, None, None, None, 0.1, None, None,
+                                 None, None, 0, None, None) == 0
+    assert so.mesh_attn_bwd_reduce(empty.handle, 1, 1, 2, 1, 128, None, None, None, None, None, None, None, 0, None,
+                                   None) == 0

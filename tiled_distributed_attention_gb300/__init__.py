@@ -39,7 +39,8 @@ P_sz = ctypes.POINTER(c_sz)
 class PlanInfo(ctypes.Structure):
     _fields_ = [("S", c_i64), ("L", c_i64), ("P", c_i32), ("R", c_i32), ("causal", c_i32), ("kvr", c_i32),
                 ("greedy", c_i32), ("n_slots", c_i32), ("n_steps", c_i32), ("layout", c_i32), ("tile_q", c_i32),
-                ("tile_kv", c_i32), ("n_kv_entries", c_i64), ("n_live_blocks", c_i64)]
+                ("tile_kv", c_i32), ("n_kv_entries", c_i64), ("n_live_blocks", c_i64), ("n_kv_slots", c_i32),
+                ("reserved", c_i32)]
 
 
 _SIGS = {
@@ -58,6 +59,14 @@ _SIGS = {
     "mesh_attn_tile_fwd_noalloc": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_f32, c_vp,
                                            c_vp, c_vp, c_vp]),
     "mesh_attn_merge": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    "mesh_attn_plan_kv_slots": (c_i32, [c_vp, P_i32, P_i32, P_i32, P_i32]),
+    "mesh_attn_bwd_partials_size": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, P_sz, P_sz]),
+    "mesh_attn_bwd_workspace_size": (c_i32, [c_vp, P_sz]),
+    "mesh_attn_bwd_prep": (c_i32, [c_i32, c_i32, c_i32, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
+    "mesh_attn_tile_bwd": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                   c_f32, c_vp, c_vp, c_vp, c_vp, c_sz, c_vp, c_vp]),
+    "mesh_attn_bwd_reduce": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                     c_vp, c_sz, c_vp, c_vp]),
     "mesh_attn_read_status": (c_i32, [c_vp, c_vp, P_i32]),
     "mesh_attn_status_string": (ctypes.c_char_p, [c_i32]),
     "mesh_attn_last_error": (ctypes.c_char_p, []),
@@ -126,7 +135,7 @@ class Plan:
 
     def __getattr__(self, name):
         if name in ("S", "L", "P", "R", "causal", "kvr", "greedy", "n_slots", "n_steps", "n_kv_entries",
-                    "n_live_blocks", "layout", "tile_q", "tile_kv"):
+                    "n_live_blocks", "layout", "tile_q", "tile_kv", "n_kv_slots"):
             return getattr(self.__dict__["info"], name)
         raise AttributeError(name)
 
@@ -263,6 +272,107 @@ def mesh_attn_merge(plan: Plan, B: int, Hq: int, d: int, partial_o: torch.Tensor
     _check(_lib.mesh_attn_merge(plan.handle, _dtype_code(O.dtype), B, Hq, d, _ptr(partial_o), _ptr(partial_lse),
                                 _ptr(O), _ptr(LSE), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                 _ptr(status), _stream_handle(stream)), "mesh_attn_merge")
+
+
+def mesh_attn_plan_kv_slots(plan: Plan):
+    """Backward KV slots: (kv_slot_off [P+1], [(k, t, kv_slot)], [[Q partitions] per slot])."""
+    n = plan.n_kv_slots
+    off, items, q_off, q_list = _i32(plan.P + 1), _i32(3 * n), _i32(n + 1), _i32(plan.n_live_blocks)
+    _check(_lib.mesh_attn_plan_kv_slots(plan.handle, off, items, q_off, q_list), "mesh_attn_plan_kv_slots")
+    qo = list(q_off[:n + 1])
+    ql = list(q_list[:plan.n_live_blocks])
+    return (list(off[:plan.P + 1]), [tuple(items[3 * i:3 * i + 3]) for i in range(n)],
+            [ql[qo[i]:qo[i + 1]] for i in range(n)])
+
+
+def mesh_attn_bwd_partials_size(plan: Plan, B: int, Hq: int, Hkv: int, d: int) -> Tuple[int, int]:
+    q, kv = c_sz(), c_sz()
+    _check(_lib.mesh_attn_bwd_partials_size(plan.handle, B, Hq, Hkv, d, ctypes.byref(q), ctypes.byref(kv)),
+           "mesh_attn_bwd_partials_size")
+    return q.value, kv.value
+
+
+def mesh_attn_bwd_workspace_size(plan: Plan) -> int:
+    n = c_sz()
+    _check(_lib.mesh_attn_bwd_workspace_size(plan.handle, ctypes.byref(n)), "mesh_attn_bwd_workspace_size")
+    return n.value
+
+
+def new_bwd_workspace(plan: Plan, device=None) -> torch.Tensor:
+    return torch.empty(max(mesh_attn_bwd_workspace_size(plan), 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def new_bwd_partials(plan: Plan, B: int, Hq: int, Hkv: int, d: int, device=None):
+    nq, nkv = mesh_attn_bwd_partials_size(plan, B, Hq, Hkv, d)
+    dev = device or "cuda"
+    return tuple(torch.empty(max(n, 4), dtype=torch.float32, device=dev) for n in (nq, nkv, nkv))
+
+
+def mesh_attn_bwd_prep(O: torch.Tensor, dO: torch.Tensor, D: torch.Tensor, status: torch.Tensor,
+                       stream=None) -> None:
+    B, Hq, S, d = O.shape
+    if O.dtype != dO.dtype or not O.is_contiguous() or not dO.is_contiguous():
+        raise ValueError("O and dO must be contiguous and of one dtype")
+    _check(_lib.mesh_attn_bwd_prep(_dtype_code(O.dtype), B, Hq, S, d, _ptr(O), _ptr(dO), _ptr(D), _ptr(status),
+                                   _stream_handle(stream)), "mesh_attn_bwd_prep")
+
+
+def mesh_attn_tile_bwd(plan: Plan, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dO: torch.Tensor,
+                       LSE: torch.Tensor, D: torch.Tensor, scale: Optional[float], dq_partial: torch.Tensor,
+                       dk_partial: torch.Tensor, dv_partial: torch.Tensor, workspace: torch.Tensor,
+                       status: torch.Tensor, stream=None) -> None:
+    B, Hq, S, d = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    for t in (q, k, v, dO):
+        if not t.is_contiguous():
+            raise ValueError("q, k, v and dO must be contiguous")
+    _check(_lib.mesh_attn_tile_bwd(plan.handle, _dtype_code(q.dtype), B, Hq, Hkv, d, _ptr(q), _ptr(k), _ptr(v),
+                                   _ptr(dO), _ptr(LSE), _ptr(D), float(scale), _ptr(dq_partial), _ptr(dk_partial),
+                                   _ptr(dv_partial), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _ptr(status), _stream_handle(stream)), "mesh_attn_tile_bwd")
+
+
+def mesh_attn_bwd_reduce(plan: Plan, B: int, Hq: int, Hkv: int, d: int, dq_partial: torch.Tensor,
+                         dk_partial: torch.Tensor, dv_partial: torch.Tensor, dQ: torch.Tensor, dK: torch.Tensor,
+                         dV: torch.Tensor, workspace: torch.Tensor, status: torch.Tensor, stream=None) -> None:
+    if not (dQ.dtype == dK.dtype == dV.dtype):
+        raise ValueError("dQ, dK and dV must share one dtype")
+    _check(_lib.mesh_attn_bwd_reduce(plan.handle, _dtype_code(dQ.dtype), B, Hq, Hkv, d, _ptr(dq_partial),
+                                     _ptr(dk_partial), _ptr(dv_partial), _ptr(dQ), _ptr(dK), _ptr(dV),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+                                     _stream_handle(stream)), "mesh_attn_bwd_reduce")
+
+
+def mesh_attention_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, O: torch.Tensor,
+                            LSE: torch.Tensor, dO: torch.Tensor, P: int, causal: bool, kvr: bool = True,
+                            greedy: bool = True, scale: Optional[float] = None, plan: Optional[Plan] = None,
+                            return_partials: bool = False, check_status: bool = True):
+    """Whole backward on the current stream: D = dO . O, tile backward, reduce.
+
+    q [B,Hq,S,d], k/v [B,Hkv,S,d], O and dO [B,Hq,S,d] (one dtype, bf16 or fp32), LSE [B,Hq,S]
+    fp32 from the forward.  Returns (dQ, dK, dV) in q's dtype; with return_partials also the
+    fp32 partials (dq, dk, dv).
+    """
+    B, Hq, S, d = q.shape
+    Hkv = k.shape[1]
+    plan = plan or mesh_attn_plan_create(S, P, causal, kvr, greedy)
+    dq_p, dk_p, dv_p = new_bwd_partials(plan, B, Hq, Hkv, d, q.device)
+    ws = new_bwd_workspace(plan, q.device)
+    st = new_status(q.device)
+    D = torch.empty(B, Hq, S, dtype=torch.float32, device=q.device)
+    dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    mesh_attn_bwd_prep(O, dO, D, st)
+    mesh_attn_tile_bwd(plan, q, k, v, dO, LSE, D, scale, dq_p, dk_p, dv_p, ws, st)
+    mesh_attn_bwd_reduce(plan, B, Hq, Hkv, d, dq_p, dk_p, dv_p, dQ, dK, dV, ws, st)
+    if check_status:
+        code = mesh_attn_read_status(st)
+        if code != 0:
+            raise MeshAttnError(code, "device", f"status block {st.tolist()}")
+    if return_partials:
+        return dQ, dK, dV, dq_p, dk_p, dv_p
+    return dQ, dK, dV
 
 
 def mesh_attn_read_status(status: torch.Tensor, stream=None) -> int:

@@ -125,6 +125,7 @@ int mesh_attn_plan_get_info(const mesh_attn_plan* plan, mesh_attn_plan_info* out
     out->tile_kv = p.tile_kv;
     out->n_kv_entries = (int64_t)p.kv_list.size();
     out->n_live_blocks = p.n_live;
+    out->n_kv_slots = p.n_kv_slots();
     return (int)MESH_ATTN_OK;
   });
 }
@@ -306,6 +307,192 @@ int mesh_attn_merge(const mesh_attn_plan* plan, mesh_attn_dtype out_dtype, int32
     std::string err;
     const int ce = mesh::launch_merge(a, out_dtype, stream, &err);
     if (ce != (int)cudaSuccess) return fail(MESH_ATTN_ERR_CUDA, err.empty() ? cudaGetErrorString((cudaError_t)ce) : err);
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_plan_kv_slots(const mesh_attn_plan* plan, int32_t* kv_slot_off, int32_t* kv_items, int32_t* q_off,
+                            int32_t* q_list) {
+  return guarded([&] {
+    if (!plan) return fail(MESH_ATTN_ERR_INVALID_ARG, "plan is NULL");
+    const mesh::Plan& p = plan->p;
+    if (kv_slot_off) std::memcpy(kv_slot_off, p.kv_slot_off.data(), p.kv_slot_off.size() * sizeof(int32_t));
+    if (kv_items) std::memcpy(kv_items, p.kv_items.data(), p.kv_items.size() * sizeof(int32_t));
+    if (q_off) std::memcpy(q_off, p.kv_q_off.data(), p.kv_q_off.size() * sizeof(int32_t));
+    if (q_list) std::memcpy(q_list, p.kv_q_list.data(), p.kv_q_list.size() * sizeof(int32_t));
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_bwd_partials_size(const mesh_attn_plan* plan, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+                                size_t* dq_elems, size_t* dkv_elems) {
+  return guarded([&] {
+    if (!plan || !dq_elems || !dkv_elems) return fail(MESH_ATTN_ERR_INVALID_ARG, "NULL argument");
+    if (B < 0 || Hq < 0 || Hkv < 0 || d < 0) return fail(MESH_ATTN_ERR_INVALID_ARG, "B, Hq, Hkv and d must be >= 0");
+    const mesh::Plan& p = plan->p;
+    *dq_elems = (size_t)B * Hq * p.n_slots() * (size_t)p.L * d;
+    *dkv_elems = (size_t)B * Hkv * p.n_kv_slots() * (size_t)p.L * d;
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_bwd_workspace_size(const mesh_attn_plan* plan, size_t* bytes) {
+  return guarded([&] {
+    if (!plan || !bytes) return fail(MESH_ATTN_ERR_INVALID_ARG, "NULL argument");
+    *bytes = mesh::bwd_workspace_layout(plan->p).total;
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_bwd_prep(mesh_attn_dtype dtype, int32_t B, int32_t Hq, int64_t S, int32_t d, const void* O,
+                       const void* dO, float* D, int32_t* d_status, void* stream) {
+  return guarded([&] {
+    if (dtype != MESH_ATTN_F32 && dtype != MESH_ATTN_BF16)
+      return fail(MESH_ATTN_ERR_INVALID_ARG, "dtype must be MESH_ATTN_F32 or MESH_ATTN_BF16");
+    if (B < 0 || Hq < 0 || S < 0) return fail(MESH_ATTN_ERR_INVALID_ARG, "B, Hq and S must be >= 0");
+    if (d != 64 && d != 128) return fail(MESH_ATTN_ERR_UNSUPPORTED, "d must be 64 or 128");
+    if (B == 0 || Hq == 0 || S == 0) return (int)MESH_ATTN_OK;
+    if (!O || !dO || !D || !d_status) return fail(MESH_ATTN_ERR_INVALID_ARG, "a tensor or status pointer is NULL");
+    if (!aligned(O, 16) || !aligned(dO, 16) || !aligned(D, 4) || !aligned(d_status, 4))
+      return fail(MESH_ATTN_ERR_MISALIGNED, "O and dO must be 16-byte aligned");
+    mesh::PrepArgs a{};
+    a.O = O;
+    a.dO = dO;
+    a.D = D;
+    a.status = d_status;
+    a.S = S;
+    a.B = B;
+    a.H = Hq;
+    a.d = d;
+    std::string err;
+    const int ce = mesh::launch_bwd_prep(a, dtype, stream, &err);
+    if (ce != (int)cudaSuccess) return fail(MESH_ATTN_ERR_CUDA, err.empty() ? cudaGetErrorString((cudaError_t)ce) : err);
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_tile_bwd(const mesh_attn_plan* plan, mesh_attn_dtype in_dtype, int32_t B, int32_t Hq, int32_t Hkv,
+                       int32_t d, const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                       const float* D, float scale, float* dq_partial, float* dk_partial, float* dv_partial,
+                       void* workspace, size_t workspace_bytes, int32_t* d_status, void* stream) {
+  return guarded([&] {
+    int rc = check_common(plan, B, Hq, d);
+    if (rc) return rc;
+    if (in_dtype != MESH_ATTN_F32 && in_dtype != MESH_ATTN_BF16)
+      return fail(MESH_ATTN_ERR_INVALID_ARG, "in_dtype must be MESH_ATTN_F32 or MESH_ATTN_BF16");
+    if (Hkv < 1 || Hq % Hkv != 0) return fail(MESH_ATTN_ERR_INVALID_ARG, "need Hkv >= 1 and Hq % Hkv == 0");
+    if (!(scale > 0.f) || !std::isfinite(scale)) return fail(MESH_ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+    const mesh::Plan& pl = plan->p;
+    if (pl.n_slots() == 0 || B == 0 || Hq == 0) return (int)MESH_ATTN_OK;
+    if (!Q || !K || !V || !dO || !LSE || !D || !dq_partial || !dk_partial || !dv_partial || !workspace || !d_status)
+      return fail(MESH_ATTN_ERR_INVALID_ARG, "a tensor, workspace or status pointer is NULL");
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(dO, 16) || !aligned(LSE, 4) ||
+        !aligned(D, 4) || !aligned(dq_partial, 16) || !aligned(dk_partial, 16) || !aligned(dv_partial, 16) ||
+        !aligned(workspace, 16) || !aligned(d_status, 4))
+      return fail(MESH_ATTN_ERR_MISALIGNED, "tensors and workspace must be 16-byte aligned");
+    const mesh::BwdWorkspaceLayout wl = mesh::bwd_workspace_layout(pl);
+    if (workspace_bytes < wl.total)
+      return fail(MESH_ATTN_ERR_WORKSPACE, "workspace needs " + std::to_string(wl.total) + " bytes");
+    char* ws = static_cast<char*>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    struct Up { size_t off; const void* src; size_t bytes; const char* what; };
+    const Up ups[] = {{wl.items_off, pl.dev_items.data(), wl.items_bytes, "work-list upload"},
+                      {wl.kv_off, pl.kv_list.data(), wl.kv_bytes, "KV-list upload"},
+                      {wl.kv_items_off, pl.dev_kv_items.data(), wl.kv_items_bytes, "KV-slot upload"},
+                      {wl.q_list_off, pl.kv_q_list.data(), wl.q_list_bytes, "Q-list upload"}};
+    for (const Up& u : ups) {
+      if (u.bytes == 0) continue;
+      cudaError_t e = cudaMemcpyAsync(ws + u.off, u.src, u.bytes, cudaMemcpyHostToDevice, st);
+      if (e != cudaSuccess) return cuda_fail(e, u.what);
+    }
+    cudaError_t e = cudaMemsetAsync(ws + wl.counter_off, 0, 512, st);  // both scheduling counters start at 0
+    if (e != cudaSuccess) return cuda_fail(e, "counter reset");
+    mesh::BwdArgs a{};
+    a.Q = Q;
+    a.K = K;
+    a.V = V;
+    a.dO = dO;
+    a.LSE = LSE;
+    a.D = D;
+    a.dq_part = dq_partial;
+    a.dk_part = dk_partial;
+    a.dv_part = dv_partial;
+    a.items = reinterpret_cast<const mesh::DevItem*>(ws + wl.items_off);
+    a.kv_list = reinterpret_cast<const int32_t*>(ws + wl.kv_off);
+    a.kv_items = reinterpret_cast<const mesh::DevItem*>(ws + wl.kv_items_off);
+    a.q_list = reinterpret_cast<const int32_t*>(ws + wl.q_list_off);
+    a.counters = reinterpret_cast<uint32_t*>(ws + wl.counter_off);
+    a.status = d_status;
+    a.S = pl.S;
+    a.L = pl.L;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.P = pl.P;
+    a.n_items = pl.n_slots();
+    a.n_slots = pl.n_slots();
+    a.n_kv_items = pl.n_kv_slots();
+    a.n_kv_slots = pl.n_kv_slots();
+    a.causal = pl.causal ? 1 : 0;
+    a.scale = scale;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    a.wait_limit_ns = g_wait_limit_ns.load();
+    std::string err;
+    const int ce = (in_dtype == MESH_ATTN_BF16) ? mesh::launch_tile_bwd_tc(a, stream, &err)
+                                                : mesh::launch_tile_bwd_simt(a, stream, &err);
+    if (ce != (int)cudaSuccess) return fail(MESH_ATTN_ERR_CUDA, err.empty() ? cudaGetErrorString((cudaError_t)ce) : err);
+    return (int)MESH_ATTN_OK;
+  });
+}
+
+int mesh_attn_bwd_reduce(const mesh_attn_plan* plan, mesh_attn_dtype out_dtype, int32_t B, int32_t Hq, int32_t Hkv,
+                         int32_t d, const float* dq_partial, const float* dk_partial, const float* dv_partial,
+                         void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes, int32_t* d_status,
+                         void* stream) {
+  return guarded([&] {
+    int rc = check_common(plan, B, Hq, d);
+    if (rc) return rc;
+    if (out_dtype != MESH_ATTN_F32 && out_dtype != MESH_ATTN_BF16)
+      return fail(MESH_ATTN_ERR_INVALID_ARG, "out_dtype must be MESH_ATTN_F32 or MESH_ATTN_BF16");
+    if (Hkv < 1 || Hq % Hkv != 0) return fail(MESH_ATTN_ERR_INVALID_ARG, "need Hkv >= 1 and Hq % Hkv == 0");
+    const mesh::Plan& pl = plan->p;
+    if (pl.S == 0 || B == 0 || Hq == 0) return (int)MESH_ATTN_OK;
+    if (!dq_partial || !dk_partial || !dv_partial || !dQ || !dK || !dV || !workspace || !d_status)
+      return fail(MESH_ATTN_ERR_INVALID_ARG, "a tensor, workspace or status pointer is NULL");
+    if (!aligned(dq_partial, 16) || !aligned(dk_partial, 16) || !aligned(dv_partial, 16) || !aligned(dQ, 16) ||
+        !aligned(dK, 16) || !aligned(dV, 16) || !aligned(workspace, 16) || !aligned(d_status, 4))
+      return fail(MESH_ATTN_ERR_MISALIGNED, "tensors and workspace must be 16-byte aligned");
+    const mesh::BwdWorkspaceLayout wl = mesh::bwd_workspace_layout(pl);
+    if (workspace_bytes < wl.total)
+      return fail(MESH_ATTN_ERR_WORKSPACE, "workspace needs " + std::to_string(wl.total) + " bytes");
+    char* ws = static_cast<char*>(workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(ws + wl.slot_off_off, pl.slot_off.data(), wl.slot_off_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "slot-offset upload");
+    e = cudaMemcpyAsync(ws + wl.kv_slot_off_off, pl.kv_slot_off.data(), wl.kv_slot_off_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "KV-slot-offset upload");
+    std::string err;
+    struct Job { const float* part; size_t off; void* out; int32_t H, n; };
+    const Job jobs[] = {{dq_partial, wl.slot_off_off, dQ, Hq, pl.n_slots()},
+                        {dk_partial, wl.kv_slot_off_off, dK, Hkv, pl.n_kv_slots()},
+                        {dv_partial, wl.kv_slot_off_off, dV, Hkv, pl.n_kv_slots()}};
+    for (const Job& j : jobs) {
+      mesh::ReduceArgs a{};
+      a.part = j.part;
+      a.off = reinterpret_cast<const int32_t*>(ws + j.off);
+      a.out = j.out;
+      a.status = d_status;
+      a.S = pl.S;
+      a.L = pl.L;
+      a.B = B;
+      a.H = j.H;
+      a.d = d;
+      a.P = pl.P;
+      a.n_slots = j.n;
+      const int ce = mesh::launch_bwd_reduce(a, out_dtype, stream, &err);
+      if (ce != (int)cudaSuccess) return fail(MESH_ATTN_ERR_CUDA, err.empty() ? cudaGetErrorString((cudaError_t)ce) : err);
+    }
     return (int)MESH_ATTN_OK;
   });
 }

@@ -35,13 +35,23 @@ struct Plan {
   std::vector<int32_t> kv_list;            // [kv_off[n]]
   std::vector<int32_t> recv;               // [P*3] Q, KV, partial-O partitions received
   std::vector<DevItem> dev_items;          // [n] the kernels' copy of the order
+  // Backward pass: the (KV partition k, tile t) pairs with a live block, grouped by k, tiles
+  // ascending; each with the tile's Q partitions live for k, ascending.
+  std::vector<int32_t> kv_slot_off;        // [P+1]
+  std::vector<int32_t> kv_items;           // [m*3] (k, t, kv slot)
+  std::vector<int32_t> kv_q_off;           // [m+1]
+  std::vector<int32_t> kv_q_list;          // [kv_q_off[m]]
+  std::vector<DevItem> dev_kv_items;       // [m] as the kernels read them: {k, kv slot, q_off, n_q}
 
   int32_t n_slots() const { return (int32_t)item_step.size(); }
+  int32_t n_kv_slots() const { return (int32_t)(kv_q_off.empty() ? 0 : kv_q_off.size() - 1); }
 };
 
 // Throws std::invalid_argument / std::bad_alloc; the ABI layer converts.
 void build_plan(Plan& plan, int64_t S, int32_t P, bool causal, bool kvr, bool greedy);
 void build_ring_plan(Plan& plan, int64_t S, int32_t P, bool causal);
+// Fills the backward fields from the tile map (called by both builders).
+void build_kv_slots(Plan& plan);
 
 // Workspace layout shared by tile_fwd and merge: [slot_off | items | kv_list | counter].
 struct WorkspaceLayout {
@@ -81,6 +91,63 @@ struct MergeArgs {
   int32_t B, Hq, d, P, n_slots;
 };
 int launch_merge(const MergeArgs& a, mesh_attn_dtype out_dtype, void* stream, std::string* err);
+
+// ---------------------------------------------------------------- backward pass
+// Workspace of the backward calls: [slot_off | items | kv_list | kv_slot_off | kv_items |
+// kv_q_list | counters (2 x 256 B)].
+struct BwdWorkspaceLayout {
+  size_t slot_off_off, slot_off_bytes, items_off, items_bytes, kv_off, kv_bytes;
+  size_t kv_slot_off_off, kv_slot_off_bytes, kv_items_off, kv_items_bytes, q_list_off, q_list_bytes;
+  size_t counter_off, total;
+};
+BwdWorkspaceLayout bwd_workspace_layout(const Plan& plan);
+
+struct BwdArgs {
+  const void* Q;
+  const void* K;
+  const void* V;
+  const void* dO;
+  const float* LSE;  // [B, Hq, S] natural log, from the forward merge
+  const float* D;    // [B, Hq, S] dO . O
+  float* dq_part;    // [B, Hq, n_slots, L, d]
+  float* dk_part;    // [B, Hkv, n_kv_slots, L, d]
+  float* dv_part;
+  const DevItem* items;     // forward work items {p, slot, kv_off, n_kv}
+  const int32_t* kv_list;
+  const DevItem* kv_items;  // KV slots {k, kv slot, q_off, n_q}
+  const int32_t* q_list;
+  uint32_t* counters;       // [2] scheduling counters (dq pass, dkdv pass)
+  int32_t* status;
+  int64_t S, L;
+  int32_t B, Hq, Hkv, d, P, n_items, n_slots, n_kv_items, n_kv_slots;
+  int32_t causal;
+  float scale;
+  float scale_log2;
+  int64_t wait_limit_ns;
+};
+int launch_tile_bwd_simt(const BwdArgs& a, void* stream, std::string* err);
+int launch_tile_bwd_tc(const BwdArgs& a, void* stream, std::string* err);
+
+struct PrepArgs {
+  const void* O;
+  const void* dO;
+  float* D;
+  int32_t* status;
+  int64_t S;
+  int32_t B, H, d;
+};
+int launch_bwd_prep(const PrepArgs& a, mesh_attn_dtype dt, void* stream, std::string* err);
+
+// out[b, h, part * L + r, :] = sum over the slots off[part] .. off[part + 1] of part[b, h, slot, r, :]
+struct ReduceArgs {
+  const float* part;
+  const int32_t* off;
+  void* out;
+  int32_t* status;
+  int64_t S, L;
+  int32_t B, H, d, P, n_slots;
+};
+int launch_bwd_reduce(const ReduceArgs& a, mesh_attn_dtype out_dtype, void* stream, std::string* err);
 
 // Record `msg` as the calling thread's last error (mesh_attn_last_error) and return `code`.
 int set_last_error(int code, const std::string& msg);

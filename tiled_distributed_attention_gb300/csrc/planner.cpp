@@ -186,6 +186,7 @@ void build_plan(Plan& pl, int64_t S, int32_t P, bool causal, bool kvr, bool gree
   }
   pl.kv_off[n] = (int32_t)pos;
   if (pos != pl.n_live) throw std::logic_error("planner: KV entries do not cover the live blocks");
+  build_kv_slots(pl);
 }
 
 // Ring-Attention's assignment in the same plan form, for comparison through the same kernels:
@@ -214,7 +215,10 @@ void build_ring_plan(Plan& pl, int64_t S, int32_t P, bool causal) {
   for (int32_t p = 0; p <= P; ++p) pl.slot_off[p] = empty ? 0 : p;
   pl.n_live = empty ? 0 : (causal ? (int64_t)P * (P + 1) / 2 : (int64_t)P * P);
   pl.recv.assign((size_t)P * 3, 0);
-  if (empty) return;
+  if (empty) {
+    build_kv_slots(pl);
+    return;
+  }
   std::vector<std::pair<int32_t, int32_t>> order;  // (completion step, device)
   order.reserve(P);
   for (int32_t v = 0; v < P; ++v) {
@@ -248,6 +252,66 @@ void build_ring_plan(Plan& pl, int64_t S, int32_t P, bool causal) {
   }
   pl.kv_off[P] = (int32_t)pos;
   if (pos != pl.n_live) throw std::logic_error("ring planner: KV entries do not cover the live blocks");
+  build_kv_slots(pl);
+}
+
+// Backward pass: tile t sums dK and dV of each of its KV partitions over its own live Q
+// partitions; those partial sums travel back along the mesh column to k's owner, as the
+// forward's partial outputs travel along the mesh row.  Slots are grouped by k, tiles ascending.
+void build_kv_slots(Plan& pl) {
+  const int32_t P = pl.P;
+  pl.kv_slot_off.assign((size_t)P + 1, 0);
+  pl.kv_items.clear();
+  pl.kv_q_off.assign(1, 0);
+  pl.kv_q_list.clear();
+  pl.dev_kv_items.clear();
+  if (pl.S == 0) return;
+  // tiles holding each KV partition, ascending (each tile lists a partition at most once)
+  std::vector<std::vector<int32_t>> holders((size_t)P);
+  for (int32_t t = 0; t < P; ++t)
+    for (int32_t i = 0; i < pl.tile_kv; ++i) holders[(size_t)pl.kv_parts[(size_t)t * pl.tile_kv + i]].push_back(t);
+  std::vector<int32_t> qs;
+  for (int32_t k = 0; k < P; ++k) {
+    for (int32_t t : holders[(size_t)k]) {
+      qs.clear();
+      for (int32_t j = 0; j < pl.tile_q; ++j) {
+        const int32_t p = pl.q_parts[(size_t)t * pl.tile_q + j];
+        if (live(p, k, pl.causal)) qs.push_back(p);
+      }
+      if (qs.empty()) continue;
+      std::sort(qs.begin(), qs.end());
+      const int32_t slot = (int32_t)pl.dev_kv_items.size();
+      pl.kv_items.push_back(k);
+      pl.kv_items.push_back(t);
+      pl.kv_items.push_back(slot);
+      pl.dev_kv_items.push_back(DevItem{k, slot, (int32_t)pl.kv_q_list.size(), (int32_t)qs.size()});
+      pl.kv_q_list.insert(pl.kv_q_list.end(), qs.begin(), qs.end());
+      pl.kv_q_off.push_back((int32_t)pl.kv_q_list.size());
+    }
+    pl.kv_slot_off[(size_t)k + 1] = (int32_t)pl.dev_kv_items.size();
+  }
+  if ((int64_t)pl.kv_q_list.size() != pl.n_live)
+    throw std::logic_error("planner: KV slots do not cover the live blocks");
+}
+
+BwdWorkspaceLayout bwd_workspace_layout(const Plan& pl) {
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  BwdWorkspaceLayout w{};
+  w.slot_off_off = 0;
+  w.slot_off_bytes = sizeof(int32_t) * pl.slot_off.size();
+  w.items_off = up(w.slot_off_bytes);
+  w.items_bytes = sizeof(DevItem) * pl.dev_items.size();
+  w.kv_off = w.items_off + up(w.items_bytes);
+  w.kv_bytes = sizeof(int32_t) * pl.kv_list.size();
+  w.kv_slot_off_off = w.kv_off + up(w.kv_bytes);
+  w.kv_slot_off_bytes = sizeof(int32_t) * pl.kv_slot_off.size();
+  w.kv_items_off = w.kv_slot_off_off + up(w.kv_slot_off_bytes);
+  w.kv_items_bytes = sizeof(DevItem) * pl.dev_kv_items.size();
+  w.q_list_off = w.kv_items_off + up(w.kv_items_bytes);
+  w.q_list_bytes = sizeof(int32_t) * pl.kv_q_list.size();
+  w.counter_off = w.q_list_off + up(w.q_list_bytes);
+  w.total = w.counter_off + 512;
+  return w;
 }
 
 WorkspaceLayout workspace_layout(const Plan& pl) {
