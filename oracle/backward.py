@@ -36,11 +36,16 @@ from oracle.attention import F64, _as64, attention_bhsd, attention_rows, default
 
 
 def bwd_rows(q, q_pos, k, v, do, lse, dsum, scale: float, causal: bool, key_pos=None,
-             key_chunk: int = 4096, want_kv: bool = True) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+             key_chunk: int = 4096, want_kv: bool = True, absolute: bool = False,
+             dmag=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Gradient sums over the (row, key) pairs of query rows q [n, d] (global positions q_pos,
     global LSE lse [n], D = dO . O dsum [n], upstream gradient do [n, dv]) and keys k [m, d],
     v [m, dv] at positions key_pos (default 0..m-1).  want_kv=False skips dk and dv (returned as
-    zeros).
+    zeros).  absolute=True returns instead the magnitudes that scale the rounding error of a
+    computation that rounds dS and P to a short format and takes D from a rounded O:
+    scale sum_j (|dS_ij| + dmag_i P_ij) |k_j|, scale sum_i (|dS_ij| + dmag_i P_ij) |q_i| and
+    sum_i P_ij |dO_i| (elementwise absolute values), with dmag [n] the rows' magnitude of D
+    (see attention_bwd_bhsd).
 
     Returns (dq [n, d], dk [m, d], dv [m, dv]) in fp64: dq_i = scale sum_j dS_ij k_j over these
     keys, dk_j = scale sum_i dS_ij q_i and dv_j = sum_i P_ij dO_i over these rows.  Rows with
@@ -67,16 +72,23 @@ def bwd_rows(q, q_pos, k, v, do, lse, dsum, scale: float, causal: bool, key_pos=
         p = torch.where(visible, p, torch.zeros_like(p))
         dp = do @ v[c0:c1].T
         ds = p * (dp - dsum[:, None])
-        dq += scale * (ds @ k[c0:c1])
+        kc, qq, dd = k[c0:c1], q, do
+        if absolute:
+            ds = ds.abs() + (0.0 if dmag is None else _as64(dmag)[:, None] * p)
+            kc, qq, dd = kc.abs(), q.abs(), do.abs()
+        dq += scale * (ds @ kc)
         if want_kv:
-            dk[c0:c1] = scale * (ds.T @ q)
-            dv[c0:c1] = p.T @ do
+            dk[c0:c1] = scale * (ds.T @ qq)
+            dv[c0:c1] = p.T @ dd
     return dq, dk, dv
 
 
-def attention_bwd_bhsd(Q, K, V, dO, causal: bool, scale: Optional[float] = None):
+def attention_bwd_bhsd(Q, K, V, dO, causal: bool, scale: Optional[float] = None, absolute: bool = False):
     """Full backward for Q [B,Hq,S,d], K/V [B,Hkv,S,d], dO [B,Hq,S,d] (any float dtype, upcast
-    exactly).  The forward quantities O, LSE come from the forward oracle.
+    exactly).  The forward quantities O, LSE come from the forward oracle.  absolute=True gives
+    the magnitude sums of bwd_rows in place of dQ, dK, dV, and in place of D the rows' magnitude
+    of D, dmag_i = sum_e |dO_ie| (|O_ie| + sum_j P_ij |v_je|): a rounding of O by a relative u
+    (plus a rounding of P by u inside O) moves D_i by at most u dmag_i.
 
     Returns dQ [B,Hq,S,d], dK, dV [B,Hkv,S,d], LSE [B,Hq,S] and D [B,Hq,S], all fp64.
     """
@@ -86,6 +98,9 @@ def attention_bwd_bhsd(Q, K, V, dO, causal: bool, scale: Optional[float] = None)
     scale = default_scale(d) if scale is None else scale
     O, LSE = attention_bhsd(Q, K, V, causal, scale)
     D = (_as64(dO) * O).sum(dim=-1)
+    if absolute:
+        O_abs, _ = attention_bhsd(Q, K, _as64(V).abs(), causal, scale)
+        D = (_as64(dO).abs() * (O.abs() + O_abs)).sum(dim=-1)
     dQ = torch.zeros(B, Hq, S, d, dtype=F64)
     dK = torch.zeros(B, Hkv, S, d, dtype=F64)
     dV = torch.zeros(B, Hkv, S, V.shape[-1], dtype=F64)
@@ -94,8 +109,9 @@ def attention_bwd_bhsd(Q, K, V, dO, causal: bool, scale: Optional[float] = None)
         for kh in range(Hkv):
             k64, v64 = _as64(K[b, kh]), _as64(V[b, kh])
             for h in range(kh * g, (kh + 1) * g):
-                dq, dk, dv = bwd_rows(_as64(Q[b, h]), pos, k64, v64, _as64(dO[b, h]), LSE[b, h], D[b, h],
-                                      scale, causal)
+                dsum = (_as64(dO[b, h]) * O[b, h]).sum(dim=-1)
+                dq, dk, dv = bwd_rows(_as64(Q[b, h]), pos, k64, v64, _as64(dO[b, h]), LSE[b, h], dsum,
+                                      scale, causal, absolute=absolute, dmag=D[b, h] if absolute else None)
                 dQ[b, h] = dq
                 dK[b, kh] += dk
                 dV[b, kh] += dv

@@ -174,3 +174,25 @@ def test_kv_slots_ring_and_empty():
     assert ks.kv_slot_off == [0, 3, 5, 6]
     empty = PL.kv_slots(PL.make_plan(0, 4, True, True, True))
     assert empty.kv_items == [] and empty.kv_slot_off == [0] * 5
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_magnitude_sums_bound_the_gradients(causal):
+    """The magnitude sums bound the gradients elementwise (triangle inequality), and equal dV when
+    every term P_ij dO_i is non-negative (dO >= 0)."""
+    Q, K, V, dO = _case(1, 4, 2, 19, 8, 61)
+    g = OB.attention_bwd_bhsd(Q, K, V, dO, causal)
+    m = OB.attention_bwd_bhsd(Q, K, V, dO, causal, absolute=True)
+    for a, b in zip(g[:3], m[:3]):
+        assert (a.abs() <= b + 1e-12).all()
+    dOp = dO.abs()
+    g = OB.attention_bwd_bhsd(Q, K, V, dOp, causal)
+    m = OB.attention_bwd_bhsd(Q, K, V, dOp, causal, absolute=True)
+    assert torch.allclose(g[2], m[2], atol=1e-12)
+    assert (m[0] > g[0].abs()).any()  # dS changes sign: the dQ magnitude is a strict bound somewhere
+    # the magnitude of D bounds |D| = |dO . O| (and equals 2 sum |dO| |O| when V >= 0)
+    assert (m[4] >= g[4].abs() - 1e-12).all()
+    Vp = V.abs()
+    O, _ = OA.attention_bhsd(Q, K, Vp, causal)
+    mp = OB.attention_bwd_bhsd(Q, K, Vp, dOp, causal, absolute=True)
+    assert torch.allclose(mp[4], 2 * (dOp * O).sum(dim=-1), atol=1e-12)

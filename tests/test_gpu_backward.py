@@ -8,16 +8,27 @@ import torch
 
 from mesh_inputs import WORKLOADS, Workload, make_do, make_qkv
 from oracle import backward as OB
-from tests.gpu_helpers import max_err
+
 
 pytestmark = pytest.mark.gpu
 
-# fp32: the fp32 tolerance of the forward (1e-4 absolute).  bf16: see BWD_TOL_BF16.
+# fp32: the fp32 tolerance of the forward (1e-4 absolute).  bf16: see bf16_bound.
 F32_CASES = [
     WORKLOADS["tiny_f32"],
     Workload(140, "f32_bwd_causal_ragged_L100", 1, 2, 1, 900, 128, "f32", True, 9),
     Workload(141, "f32_bwd_gqa_d64", 1, 4, 2, 512, 64, "f32", False, 4),
     Workload(142, "f32_bwd_batch2_causal", 2, 2, 2, 256, 64, "f32", True, 4),
+]
+
+
+BF16_CASES = [
+    Workload(150, "bf16_bwd_causal_L1024", 1, 2, 2, 4096, 128, "bf16", True, 4),
+    Workload(151, "bf16_bwd_gqa_noncausal", 1, 4, 2, 2048, 128, "bf16", False, 4),
+    Workload(152, "bf16_bwd_ragged_L200_causal", 1, 2, 1, 800, 128, "bf16", True, 4),
+    Workload(153, "bf16_bwd_d64_P9", 1, 2, 2, 3456, 64, "bf16", True, 9),
+    Workload(154, "bf16_bwd_batch2_ragged_d64", 2, 2, 1, 900, 64, "bf16", False, 9),
+    Workload(155, "bf16_bwd_single_partition", 1, 2, 1, 640, 128, "bf16", True, 1),
+    Workload(156, "bf16_bwd_peaked_k4", 1, 2, 1, 2048, 128, "bf16", True, 16, k_scale=4.0),
 ]
 
 
@@ -30,27 +41,33 @@ def run_backward(lib, w, q, k, v, dO, plan=None):
     return out, plan, LSE
 
 
-def bwd_tol(w, ref):
+def bf16_bound(ref, mag):
+    """Elementwise error bound of a bf16 gradient, derived from the arithmetic.  bf16 keeps 8
+    significant bits, so rounding to nearest moves a value by at most u = 2^-8 of itself.  The
+    products take P (for dV) and dS (for dQ, dK) rounded to bf16, and D comes from the forward's
+    bf16 O (off by at most u dmag); so a gradient is off by at most u mag (mag: the oracle's
+    magnitude sums, which carry both terms), and the result is rounded to bf16 once more
+    (u |ref|).  The bound is twice that, plus 1e-6 for fp32 accumulation."""
+    return 2.0 ** -7 * (mag + ref.abs()) + 1e-6
+
+
+def compare(w, got, ref, mag):
+    """(max |err|, max err / bound) of one gradient tensor."""
+    e = (got.double().cpu() - ref).abs()
     if w.dtype == "f32":
-        return 1e-4
-    return BWD_TOL_BF16(ref)
-
-
-def BWD_TOL_BF16(ref):
-    """bf16 gradients: products take bf16 P and dS, and dQ / dK / dV are rounded to bf16 at the
-    end (half an ulp: 2^-9 of the value); absolute error <= 2^-7 of the largest gradient
-    magnitude, and at least 2e-3."""
-    return max(2e-3, ref.abs().max().item() * 2.0 ** -7)
+        return e.max().item(), e.max().item() / 1e-4
+    return e.max().item(), (e / bf16_bound(ref, mag)).max().item()
 
 
 def check_gradients(w, got, q, k, v, dO, tag=""):
     dQ, dK, dV = got[:3]
     rQ, rK, rV, _, _ = OB.attention_bwd_bhsd(q, k, v, dO, w.causal)
-    for name, g, r in (("dQ", dQ, rQ), ("dK", dK, rK), ("dV", dV, rV)):
-        e = max_err(g, r)
-        t = bwd_tol(w, r)
-        print(f"[parity-bwd] {w.name}{tag} {name}: max|err| = {e:.3e} (tol {t:.3e}, max|ref| {r.abs().max().item():.3e})")
-        assert e <= t, f"{w.name} {name}: {e:.3e} > {t:.3e}"
+    mags = OB.attention_bwd_bhsd(q, k, v, dO, w.causal, absolute=True)[:3] if w.dtype == "bf16" else (None,) * 3
+    for name, g, r, m in (("dQ", dQ, rQ, mags[0]), ("dK", dK, rK, mags[1]), ("dV", dV, rV, mags[2])):
+        e, ratio = compare(w, g, r, m)
+        print(f"[parity-bwd] {w.name}{tag} {name}: max|err| = {e:.3e}, max err/bound = {ratio:.3f} "
+              f"(max|ref| {r.abs().max().item():.3e})")
+        assert ratio <= 1.0, f"{w.name} {name}: error {ratio:.3f}x the bound"
 
 
 def check_backward_partials(lib, w, plan, got, q, k, v, dO, LSE):
@@ -67,36 +84,49 @@ def check_backward_partials(lib, w, plan, got, q, k, v, dO, LSE):
     dk_p = dk_p[: B * Hkv * m * L * d].view(B, Hkv, m, L, d).cpu()
     dv_p = dv_p[: B * Hkv * m * L * d].view(B, Hkv, m, L, d).cpu()
     _, _, _, LSE64, D64 = OB.attention_bwd_bhsd(q, k, v, dO, w.causal)
+    DM64 = OB.attention_bwd_bhsd(q, k, v, dO, w.causal, absolute=True)[4] if w.dtype == "bf16" else None
     items, _, kvs = lib.mesh_attn_plan_order(plan)
     _, kv_items, kv_q = lib.mesh_attn_plan_kv_slots(plan)
     scale = 1.0 / math.sqrt(d)
-    tol = 1e-4 if w.dtype == "f32" else None
+    bf = w.dtype == "bf16"
+
+    def ok(got_, ref_, mag_):
+        e = (got_.double() - ref_).abs()
+        return bool((e <= (bf16_bound(ref_, mag_) if bf else 1e-4)).all())
+
     for b in range(B):
         for hk in range(Hkv):
             K64, V64 = k[b, hk].double(), v[b, hk].double()
             acc_k = {s: torch.zeros(L, d, dtype=torch.float64) for _, _, s in kv_items}
             acc_v = {s: torch.zeros(L, d, dtype=torch.float64) for _, _, s in kv_items}
+            mag_k = {s: torch.zeros(L, d, dtype=torch.float64) for _, _, s in kv_items}
+            mag_v = {s: torch.zeros(L, d, dtype=torch.float64) for _, _, s in kv_items}
             for h in range(hk * g, (hk + 1) * g):
                 Q64, G64 = q[b, h].double(), dO[b, h].double()
                 for (p, t, slot), kl in zip(items, kvs):
                     rows = torch.arange(p * L, (p + 1) * L)
                     keys = torch.cat([torch.arange(x * L, (x + 1) * L) for x in kl])
-                    r, _, _ = OB.bwd_rows(Q64[rows], rows, K64[keys], V64[keys], G64[rows], LSE64[b, h, rows],
-                                          D64[b, h, rows], scale, w.causal, key_pos=keys, want_kv=False)
-                    t_ = tol or BWD_TOL_BF16(r)
-                    assert max_err(dq_p[b, h, slot], r) <= t_, f"dq slot {slot} (p={p}, t={t})"
+                    args = (Q64[rows], rows, K64[keys], V64[keys], G64[rows], LSE64[b, h, rows], D64[b, h, rows],
+                            scale, w.causal)
+                    r, _, _ = OB.bwd_rows(*args, key_pos=keys, want_kv=False)
+                    m = OB.bwd_rows(*args, key_pos=keys, want_kv=False, absolute=True,
+                                    dmag=DM64[b, h, rows])[0] if bf else None
+                    assert ok(dq_p[b, h, slot], r, m), f"dq slot {slot} (p={p}, t={t})"
                 for (kk, t, slot), ql in zip(kv_items, kv_q):
                     keys = torch.arange(kk * L, (kk + 1) * L)
                     rows = torch.cat([torch.arange(x * L, (x + 1) * L) for x in ql])
-                    _, rk, rv = OB.bwd_rows(Q64[rows], rows, K64[keys], V64[keys], G64[rows], LSE64[b, h, rows],
-                                            D64[b, h, rows], scale, w.causal, key_pos=keys)
+                    args = (Q64[rows], rows, K64[keys], V64[keys], G64[rows], LSE64[b, h, rows], D64[b, h, rows],
+                            scale, w.causal)
+                    _, rk, rv = OB.bwd_rows(*args, key_pos=keys)
                     acc_k[slot] += rk
                     acc_v[slot] += rv
+                    if bf:
+                        _, mk, mv = OB.bwd_rows(*args, key_pos=keys, absolute=True, dmag=DM64[b, h, rows])
+                        mag_k[slot] += mk
+                        mag_v[slot] += mv
             for (kk, t, slot) in kv_items:
-                tk = tol or BWD_TOL_BF16(acc_k[slot])
-                tv = tol or BWD_TOL_BF16(acc_v[slot])
-                assert max_err(dk_p[b, hk, slot], acc_k[slot]) <= tk, f"dk slot {slot} (k={kk}, t={t})"
-                assert max_err(dv_p[b, hk, slot], acc_v[slot]) <= tv, f"dv slot {slot} (k={kk}, t={t})"
+                assert ok(dk_p[b, hk, slot], acc_k[slot], mag_k[slot]), f"dk slot {slot} (k={kk}, t={t})"
+                assert ok(dv_p[b, hk, slot], acc_v[slot], mag_v[slot]), f"dv slot {slot} (k={kk}, t={t})"
 
 
 @pytest.mark.parametrize("w", F32_CASES, ids=lambda w: w.name)
@@ -131,3 +161,26 @@ def test_backward_f32_closed_form_constant_values(lib):
     dO = make_do(w)
     got, _, _ = run_backward(lib, w, q, k, v, dO)
     assert got[0].abs().max().item() <= 1e-5 and got[1].abs().max().item() <= 1e-5
+
+
+@pytest.mark.parametrize("w", BF16_CASES, ids=lambda w: w.name)
+def test_backward_bf16_against_oracle(lib, w):
+    q, k, v = make_qkv(w)
+    dO = make_do(w)
+    got, plan, LSE = run_backward(lib, w, q, k, v, dO)
+    assert got[0].dtype == torch.bfloat16
+    check_gradients(w, got, q, k, v, dO)
+    if w.S <= 2048:
+        check_backward_partials(lib, w, plan, got, q, k, v, dO, LSE)
+
+
+def test_backward_bf16_plan_variants(lib):
+    w = BF16_CASES[2]
+    q, k, v = make_qkv(w)
+    dO = make_do(w)
+    for kvr, greedy in ((0, 0), (0, 1)):
+        plan = lib.mesh_attn_plan_create(w.S, w.P, w.causal, kvr, greedy)
+        got, _, _ = run_backward(lib, w, q, k, v, dO, plan=plan)
+        check_gradients(w, got, q, k, v, dO, tag=f" kvr={kvr} greedy={greedy}")
+    got, _, _ = run_backward(lib, w, q, k, v, dO, plan=lib.mesh_attn_plan_create_ring(w.S, w.P, w.causal))
+    check_gradients(w, got, q, k, v, dO, tag=" ring")

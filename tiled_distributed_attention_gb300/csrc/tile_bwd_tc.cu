@@ -1,10 +1,832 @@
-// placeholder: replaced by the tensor-core backward kernels
+// Tile attention backward on the 5th-generation tensor cores (sm_103a), bf16 inputs.
+//
+// The gradients of the forward definition (the left-hand side of "环形注意力：突破长序列处理
+// 瓶颈的分布式计算范式", §"理论奠基"), per tile of the Mesh-Attention plan ("Mesh-Attention: A New
+// Communication-Efficient Distributed Attention with Improved Data Locality", tutorial
+// §"Mesh-Attention：从一维'环'到二维'网'"), with the forward's global LSE and D_i = dO_i . O_i:
+//   P_ij = exp(s_ij - LSE_i),  dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - D_i),
+//   dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j.
+// Two kernels; one CTA owns one 128-row tile of one unit (no persistence) with 6 warps:
+//   warps 0-3  elementwise: one thread per TMEM lane (a key row in dkdv, a query row in dq)
+//   warp 4     MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M = N = 128, K = 16, issued by an
+//              elected lane of the converged warp; completion by tcgen05.commit
+//   warp 5     producer: TMA loads of 128 x 64 bf16 boxes with 128-byte swizzle
+//
+// dkdv (unit = KV slot, batch, KV head, 128-key block): K and V stay in shared memory; Q and dO
+// blocks of the slot's query rows (over the KV head's query heads) stream through two stages.
+//   TMEM: S^T | dP^T | dV | dK   (S^T = K Q^T and dP^T = V dO^T have lanes = keys; P^T and dS^T
+//   are written back as bf16 into the first half of their columns and feed dV += P^T dO and
+//   dK += dS^T Q from TMEM).  Issue order per query block i:
+//     [P^T(i) ready] dV(i), S^T(i+1)   [dS^T(i) ready] dK(i), dP^T(i+1)
+//   so the exponentials of block i+1 overlap dK(i) and dP^T(i+1), and dS^T(i+1) overlaps
+//   dV(i+1) and S^T(i+2).  LSE and D of the block's query columns are broadcast from shared
+//   memory.
+// dq (unit = forward work item, batch, head, 128-row block): Q and dO stay in shared memory; K
+//   and V blocks of the item's KV partitions stream through two stages.
+//   TMEM: S(even) | S(odd) | dP | dQ: S(j+2) is issued as soon as its K block has landed, so
+//   the exponentials of block j+1 run while dQ(j) and dP(j+1) execute.  LSE and D of a row are
+//   thread-local.
+// Every mbarrier wait is bounded; a timeout records MESH_ATTN_ERR_DEVICE_TIMEOUT, the CTA stops,
+// drains its copies and products and frees its tensor memory.
+#include <cuda.h>
 #include <cuda_runtime.h>
+
 #include <string>
+
 #include "internal.h"
+#include "ptx.cuh"
+
 namespace mesh {
-int launch_tile_bwd_tc(const BwdArgs&, void*, std::string* err) {
-  *err = "bf16 backward not built yet";
-  return (int)cudaErrorNotSupported;
+namespace btc {
+
+constexpr int BM = 128;  // rows per tile = TMEM lanes = keys / queries per block
+constexpr int NUM_THREADS = 192;
+constexpr int WARP_MMA = 4;
+constexpr int WARP_LOAD = 5;
+constexpr int64_t DRAIN_NS = 200000000;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr int ROLE_EW = 1, ROLE_MMA = 2, ROLE_LOAD = 3, ROLE_ITEM = 4;
+
+struct Params {
+  const DevItem* items;
+  const int32_t* kv_list;
+  const DevItem* kv_items;
+  const int32_t* q_list;
+  const float* lse;
+  const float* dsum;
+  float* dq_part;
+  float* dk_part;
+  float* dv_part;
+  int32_t* status;
+  int64_t S, L;
+  int32_t B, Hq, Hkv, P, n_items, n_slots, n_kv_items, n_kv_slots, nb, causal;
+  float scale, scale_log2;
+  int64_t wait_limit_ns;
+};
+
+template <int D>
+struct Layout {
+  static constexpr uint32_t TILE = BM * D * 2;  // one 128-row bf16 block
+  static constexpr uint32_t BOX = BM * 64 * 2;  // one 128 x 64 TMA box
+  // resident pair (K, V in dkdv; Q, dO in dq), then two stages of the streamed pair
+  static constexpr uint32_t RES0 = 0, RES1 = TILE, STR0 = 2 * TILE;  // stage s: STR0 + s*2*TILE (+TILE)
+  static constexpr uint32_t VEC_OFF = STR0 + 4 * TILE;  // dkdv: lse2[2][128], dsum[2][128] fp32
+  static constexpr uint32_t BAR_OFF = VEC_OFF + 4 * BM * 4;
+  static constexpr int B_RES = 0, B_FULL = 1, B_EMPTY = 3, B_S = 5, B_DP = 7, B_P = 8, B_DS = 9, B_ACC = 10,
+                       B_DRAIN = 11, B_VEC = 12, NBARS = 14;
+  static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag
+  static constexpr uint32_t TOTAL = MISC_OFF + 16;
+  static constexpr uint32_t ALLOC = TOTAL + 1024;
+};
+
+// 128-row blocks of partition `k` (keys, dq kernel) visited by query block `qb` of partition
+// `p`: on the causal diagonal partition only blocks up to the query block.
+__device__ __forceinline__ int kblocks_of(int k, int p, int causal, int nb, int qb) {
+  return (causal && k == p) ? min(nb, qb + 1) : nb;
 }
+// query blocks of partition `p` visited by key block `kb` of partition `k` (dkdv kernel)
+__device__ __forceinline__ int qblock_begin(int k, int p, int causal, int kb) { return (causal && k == p) ? kb : 0; }
+
+// Descriptor offsets (16-byte units) of a 128-row operand made of 64-column SW128 boxes.
+template <int D>
+__device__ __forceinline__ uint64_t kmaj_off(int kk) {
+  return (uint64_t)((kk >> 2) * (Layout<D>::BOX >> 4) + (kk & 3) * 2);
+}
+
+// ================================================================== dK / dV
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                    const Params prm) {
+  using Ly = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sb - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return sb + Ly::BAR_OFF + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::MISC_OFF);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + Ly::MISC_OFF + 4);
+  float* lse_s = reinterpret_cast<float*>(smem + Ly::VEC_OFF);  // [2][BM] LSE * log2 e
+  float* dsum_s = lse_s + 2 * BM;                               // [2][BM]
+  const int64_t L = prm.L;
+
+  // unit -> (KV slot, batch, KV head, key block)
+  int64_t uu = blockIdx.x;
+  const int kb = (int)(uu % prm.nb); uu /= prm.nb;
+  const int hk = (int)(uu % prm.Hkv); uu /= prm.Hkv;
+  const int b = (int)(uu % prm.B);
+  const int idx = (int)(uu / prm.B);
+  const DevItem it = prm.kv_items[idx];  // {k, kv slot, q_off, n_q}
+  const bool unit_ok = it.p >= 0 && it.p < prm.P && it.slot >= 0 && it.slot < prm.n_kv_slots && it.n_kv >= 1 &&
+                       it.kv_off >= 0;
+  const int k = it.p;
+  const int g = prm.Hq / prm.Hkv;
+  // query blocks of the unit: heads of the group x Q partitions of the slot x blocks
+  int NBQ = 0;
+  if (unit_ok)
+    for (int qi = 0; qi < it.n_kv; ++qi) {
+      const int p = __ldg(prm.q_list + it.kv_off + qi);
+      NBQ += prm.nb - qblock_begin(k, p, prm.causal, kb);
+    }
+  NBQ *= g;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(Ly::B_RES), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(Ly::B_FULL + s), 1);
+      mbar_init(bar(Ly::B_EMPTY + s), 1);
+    }
+    mbar_init(bar(Ly::B_S), 1);
+    mbar_init(bar(Ly::B_S + 1), 1);
+    mbar_init(bar(Ly::B_DP), 1);
+    mbar_init(bar(Ly::B_P), 4);   // one lane of each elementwise warp
+    mbar_init(bar(Ly::B_DS), 4);
+    mbar_init(bar(Ly::B_ACC), 1);
+    mbar_init(bar(Ly::B_DRAIN), 1);
+    mbar_init(bar(Ly::B_VEC), BM);  // every elementwise thread has written its LSE / D value
+    mbar_init(bar(Ly::B_VEC + 1), BM);
+    *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0 || !unit_ok) ? 1 : 0;
+    if (!unit_ok) record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_ITEM, (int32_t)blockIdx.x);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == WARP_LOAD && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmG);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool run = *abort_flag == 0;
+
+  // the i-th query block of the unit: head, partition, block
+  auto block_at = [&](int i, int& h, int& p, int& qb) {
+    const int per_head = NBQ / g;
+    h = hk * g + i / per_head;
+    int r = i % per_head;
+    for (int qi = 0; qi < it.n_kv; ++qi) {
+      p = __ldg(prm.q_list + it.kv_off + qi);
+      const int b0 = qblock_begin(k, p, prm.causal, kb);
+      if (r < prm.nb - b0) {
+        qb = b0 + r;
+        return;
+      }
+      r -= prm.nb - b0;
+    }
+    p = -1;
+    qb = 0;
+  };
+
+  if (warp < 4) {
+    // ================================================================ elementwise
+    const int row = warp * 32 + lane;  // TMEM lane = key row within the block
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t tm_s = tmem + lane_base;             // S^T, then P^T (bf16) in its first half
+    const uint32_t tm_dp = tmem + lane_base + 128u;     // dP^T, then dS^T (bf16)
+    const uint32_t tm_dv = tmem + lane_base + 256u;
+    const uint32_t tm_dk = tmem + lane_base + 256u + (uint32_t)D;
+    const int64_t key_local = (int64_t)kb * BM + row;
+    bool ok = run;
+    // LSE / D of the next block's query columns, loaded one block ahead by thread `row`
+    float nxt_lse = 0.f, nxt_d = 0.f;
+    auto fetch = [&](int i) {
+      int h, p, qb;
+      block_at(i, h, p, qb);
+      const int64_t ql = (int64_t)qb * BM + row;
+      if (p >= 0 && p < prm.P && ql < L) {
+        const int64_t gi = ((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + ql;
+        nxt_lse = __ldg(prm.lse + gi) * LOG2E;
+        nxt_d = __ldg(prm.dsum + gi);
+      } else {
+        nxt_lse = INFINITY;  // no row: exp2(s - inf) = 0
+        nxt_d = 0.f;
+      }
+    };
+    if (ok && NBQ > 0) fetch(0);
+    for (int i = 0; i < NBQ && ok; ++i) {
+      const int vb = i & 1;
+      // publish this row's LSE / D, then wait (bounded) until all 128 columns are written; a
+      // buffer is rewritten two blocks later, after every thread has arrived for the block between
+      lse_s[vb * BM + row] = nxt_lse;
+      dsum_s[vb * BM + row] = nxt_d;
+      mbar_arrive(bar(Ly::B_VEC + vb));
+      if (i + 1 < NBQ) fetch(i + 1);
+      ok = mbar_wait(bar(Ly::B_VEC + vb), (uint32_t)((i >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                     ROLE_EW, i);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      int h, p, qb;
+      block_at(i, h, p, qb);
+      (void)h;
+      // visible query columns of this key row: [lo, hi)
+      const int64_t qvalid = L - (int64_t)qb * BM;
+      const int hi = (int)min((int64_t)BM, qvalid);
+      const int lo = (prm.causal && p == k && qb == kb) ? row : 0;
+      ok = mbar_wait(bar(Ly::B_S), (uint32_t)(i & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, i);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float pv[BM];
+#pragma unroll
+      for (int c = 0; c < BM; c += 32) tmem_ld32(tm_s + (uint32_t)c, pv + c);
+      tc_wait_ld();
+      const float* lv = lse_s + vb * BM;
+      const bool full = (lo == 0 && hi == BM) || key_local >= L;
+      uint32_t pk[BM / 2];
+#pragma unroll
+      for (int c = 0; c < BM; c += 2) {
+        const float2 l2 = *reinterpret_cast<const float2*>(lv + c);
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), f2_pack(prm.scale_log2, prm.scale_log2),
+                         f2_pack(-l2.x, -l2.y)),
+                  x0, x1);
+        float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+        if (!full) {
+          p0 = (c >= lo && c < hi) ? p0 : 0.f;
+          p1 = (c + 1 >= lo && c + 1 < hi) ? p1 : 0.f;
+        }
+        pv[c] = p0;
+        pv[c + 1] = p1;
+        pk[c / 2] = pack_bf16x2(p0, p1);
+      }
+      tmem_st32(tm_s, pk);
+      tmem_st32(tm_s + 32u, pk + 32);
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Ly::B_P));
+      ok = mbar_wait(bar(Ly::B_DP), (uint32_t)(i & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, i);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float* dv_ = dsum_s + vb * BM;
+#pragma unroll
+      for (int c0 = 0; c0 < BM; c0 += 64) {
+        float dp[64];
+        tmem_ld32(tm_dp + (uint32_t)c0, dp);
+        tmem_ld32(tm_dp + (uint32_t)c0 + 32u, dp + 32);
+        tc_wait_ld();
+        uint32_t dk2[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float2 d2 = *reinterpret_cast<const float2*>(dv_ + c0 + c);
+          float a0, a1;
+          f2_unpack(f2_add(f2_pack(dp[c], dp[c + 1]), f2_pack(-d2.x, -d2.y)), a0, a1);
+          dk2[c / 2] = pack_bf16x2(pv[c0 + c] * a0, pv[c0 + c + 1] * a1);
+        }
+        // dS^T columns c0 .. c0 + 63 -> packed TMEM columns c0/2 .. c0/2 + 31 of the dP^T region
+        // (those dP^T columns were read above, and later chunks read columns >= c0 + 64)
+        tmem_st32(tm_dp + (uint32_t)(c0 / 2), dk2);
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Ly::B_DS));
+    }
+    // ---- epilogue: dV and dK rows of this key block
+    if (ok) {
+      ok = mbar_wait(bar(Ly::B_ACC), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, -1);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const int64_t prow = (((int64_t)b * prm.Hkv + hk) * prm.n_kv_slots + it.slot) * L + key_local;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        float v[32], kk[32];
+        tmem_ld32(tm_dv + (uint32_t)c, v);
+        tmem_ld32(tm_dk + (uint32_t)c, kk);
+        tc_wait_ld();
+        if (key_local < L) {
+          float4* dvp = reinterpret_cast<float4*>(prm.dv_part + prow * D + c);
+          float4* dkp = reinterpret_cast<float4*>(prm.dk_part + prow * D + c);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            dvp[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+            dkp[e] = make_float4(kk[4 * e] * prm.scale, kk[4 * e + 1] * prm.scale, kk[4 * e + 2] * prm.scale,
+                                 kk[4 * e + 3] * prm.scale);
+          }
+        }
+      }
+    }
+  } else if (warp == WARP_MMA) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t idesc_ss = idesc_bf16_f32(BM, BM, false);  // S^T, dP^T: K-major A and B
+    constexpr uint32_t idesc_ts = idesc_bf16_f32(BM, D, true);    // dV, dK: B MN-major
+    const uint64_t kdesc = smem_desc_sw128(sb + Ly::RES0, 16u, 1024u);
+    const uint64_t vdesc = smem_desc_sw128(sb + Ly::RES1, 16u, 1024u);
+    constexpr uint64_t TILE16 = Ly::TILE >> 4;
+    const uint64_t str_kmaj = smem_desc_sw128(sb + Ly::STR0, 16u, 1024u);
+    const uint64_t str_mn = smem_desc_sw128(sb + Ly::STR0, Ly::BOX, 1024u);
+    // stage s: Q at STR0 + 2 s TILE, dO at STR0 + (2 s + 1) TILE
+    auto issue_s = [&](int s) {  // S^T = K Q^T
+      const uint64_t qd = str_kmaj + (uint64_t)(2 * s) * TILE16;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        tc_mma_ss_warp(tmem, kdesc + kmaj_off<D>(kk), qd + kmaj_off<D>(kk), idesc_ss, kk > 0);
+      tc_commit_warp(bar(Ly::B_S));
+    };
+    auto issue_dp = [&](int s) {  // dP^T = V dO^T
+      const uint64_t gd = str_kmaj + (uint64_t)(2 * s + 1) * TILE16;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        tc_mma_ss_warp(tmem + 128u, vdesc + kmaj_off<D>(kk), gd + kmaj_off<D>(kk), idesc_ss, kk > 0);
+      tc_commit_warp(bar(Ly::B_DP));
+    };
+    auto issue_dv = [&](int s, bool first) {  // dV += P^T dO
+      const uint64_t gd = str_mn + (uint64_t)(2 * s + 1) * TILE16;
+#pragma unroll
+      for (int kk = 0; kk < BM / 16; ++kk)
+        tc_mma_ts_warp(tmem + 256u, tmem + (uint32_t)(kk * 8), gd + (uint64_t)(kk * 128), idesc_ts,
+                       (!first || kk > 0) ? 1u : 0u);
+    };
+    auto issue_dk = [&](int s, bool first) {  // dK += dS^T Q
+      const uint64_t qd = str_mn + (uint64_t)(2 * s) * TILE16;
+#pragma unroll
+      for (int kk = 0; kk < BM / 16; ++kk)
+        tc_mma_ts_warp(tmem + 256u + (uint32_t)D, tmem + 128u + (uint32_t)(kk * 8), qd + (uint64_t)(kk * 128),
+                       idesc_ts, (!first || kk > 0) ? 1u : 0u);
+    };
+    bool ok = run && NBQ > 0;
+    if (ok) ok = mbar_wait_warp(bar(Ly::B_RES), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, -1);
+    if (ok) ok = mbar_wait_warp(bar(Ly::B_FULL), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, 0);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0);
+      issue_dp(0);
+    }
+    for (int i = 0; i < NBQ && ok; ++i) {
+      const int s = i & 1, sn = (i + 1) & 1;
+      ok = mbar_wait_warp(bar(Ly::B_P), (uint32_t)(i & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, i);
+      if (!ok) break;
+      tc_fence_after();
+      issue_dv(s, i == 0);
+      if (i + 1 < NBQ) {
+        ok = mbar_wait_warp(bar(Ly::B_FULL + sn), (uint32_t)(((i + 1) >> 1) & 1), prm.wait_limit_ns, abort_flag,
+                            prm.status, ROLE_MMA, i + 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(sn);
+      }
+      ok = mbar_wait_warp(bar(Ly::B_DS), (uint32_t)(i & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, i);
+      if (!ok) break;
+      tc_fence_after();
+      issue_dk(s, i == 0);
+      tc_commit_warp(bar(Ly::B_EMPTY + s));  // Q(i) and dO(i) are no longer read
+      if (i + 1 < NBQ) issue_dp(sn);
+    }
+    if (ok) tc_commit_warp(bar(Ly::B_ACC));
+    tc_commit_warp(bar(Ly::B_DRAIN));
+    mbar_drain(bar(Ly::B_DRAIN), 0u, DRAIN_NS);
+  } else if (warp == WARP_LOAD && lane == 0) {
+    // ================================================================ producer
+    bool ok = run && NBQ > 0;
+    const int64_t kvrow = ((int64_t)b * prm.Hkv + hk) * prm.S + (int64_t)k * L + (int64_t)kb * BM;
+    int issued = 0;
+    if (ok) {
+      mbar_expect_tx(bar(Ly::B_RES), 2 * Ly::TILE);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_2d(sb + Ly::RES0 + (uint32_t)c * Ly::BOX, &tmK, c * 64, (int32_t)kvrow, bar(Ly::B_RES));
+        tma_load_2d(sb + Ly::RES1 + (uint32_t)c * Ly::BOX, &tmV, c * 64, (int32_t)kvrow, bar(Ly::B_RES));
+      }
+    }
+    for (int i = 0; i < NBQ && ok; ++i) {
+      const int s = i & 1;
+      if (i >= 2) {
+        ok = mbar_wait(bar(Ly::B_EMPTY + s), (uint32_t)(((i >> 1) - 1) & 1), prm.wait_limit_ns, abort_flag,
+                       prm.status, ROLE_LOAD, i);
+        if (!ok) break;
+      }
+      int h, p, qb;
+      block_at(i, h, p, qb);
+      if (p < 0 || p >= prm.P) {
+        record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_LOAD, (int32_t)blockIdx.x);
+        *abort_flag = 1;
+        break;
+      }
+      const int32_t qrow = (int32_t)(((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + (int64_t)qb * BM);
+      mbar_expect_tx(bar(Ly::B_FULL + s), 2 * Ly::TILE);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_2d(sb + Ly::STR0 + (uint32_t)(2 * s) * Ly::TILE + (uint32_t)c * Ly::BOX, &tmQ, c * 64, qrow,
+                    bar(Ly::B_FULL + s));
+        tma_load_2d(sb + Ly::STR0 + (uint32_t)(2 * s + 1) * Ly::TILE + (uint32_t)c * Ly::BOX, &tmG, c * 64, qrow,
+                    bar(Ly::B_FULL + s));
+      }
+      ++issued;
+    }
+    // exit-path drain: every load issued lands before the CTA exits
+    if (run && NBQ > 0) mbar_drain(bar(Ly::B_RES), 0u, DRAIN_NS);
+    for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
+      mbar_drain(bar(Ly::B_FULL + (j & 1)), (uint32_t)((j >> 1) & 1), DRAIN_NS);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================== dQ
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
+                  const Params prm) {
+  using Ly = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sb - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return sb + Ly::BAR_OFF + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::MISC_OFF);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + Ly::MISC_OFF + 4);
+  const int64_t L = prm.L;
+
+  // unit -> (work item, batch, head, query block)
+  int64_t uu = blockIdx.x;
+  const int qb = (int)(uu % prm.nb); uu /= prm.nb;
+  const int h = (int)(uu % prm.Hq); uu /= prm.Hq;
+  const int b = (int)(uu % prm.B);
+  const int idx = (int)(uu / prm.B);
+  const DevItem it = prm.items[idx];  // {p, slot, kv_off, n_kv}
+  const bool unit_ok = it.p >= 0 && it.p < prm.P && it.slot >= 0 && it.slot < prm.n_slots && it.n_kv >= 1 &&
+                       it.kv_off >= 0;
+  const int p = it.p;
+  const int hk = h / (prm.Hq / prm.Hkv);
+  int NB = 0;
+  if (unit_ok)
+    for (int ki = 0; ki < it.n_kv; ++ki) NB += kblocks_of(__ldg(prm.kv_list + it.kv_off + ki), p, prm.causal, prm.nb, qb);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(Ly::B_RES), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(Ly::B_FULL + s), 1);
+      mbar_init(bar(Ly::B_EMPTY + s), 1);
+      mbar_init(bar(Ly::B_S + s), 1);
+    }
+    mbar_init(bar(Ly::B_DP), 1);
+    mbar_init(bar(Ly::B_P), 4);
+    mbar_init(bar(Ly::B_DS), 4);
+    mbar_init(bar(Ly::B_ACC), 1);
+    mbar_init(bar(Ly::B_DRAIN), 1);
+    *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0 || !unit_ok) ? 1 : 0;
+    if (!unit_ok) record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_ITEM, (int32_t)blockIdx.x);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == WARP_LOAD && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmG);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool run = *abort_flag == 0;
+
+  // the j-th key block of the unit: KV partition and block
+  auto block_at = [&](int j, int& kp, int& kbk) {
+    int r = j;
+    for (int ki = 0; ki < it.n_kv; ++ki) {
+      kp = __ldg(prm.kv_list + it.kv_off + ki);
+      const int n = kblocks_of(kp, p, prm.causal, prm.nb, qb);
+      if (r < n) {
+        kbk = r;
+        return;
+      }
+      r -= n;
+    }
+    kp = -1;
+    kbk = 0;
+  };
+
+  if (warp < 4) {
+    // ================================================================ elementwise
+    const int row = warp * 32 + lane;  // TMEM lane = query row within the block
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t tm_dp = tmem + lane_base + 256u;  // dP, then dS (bf16)
+    const uint32_t tm_dq = tmem + lane_base + 384u;
+    const int64_t q_local = (int64_t)qb * BM + row;
+    const int64_t grow = ((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + q_local;
+    const bool row_in = q_local < L;
+    const float lse2 = row_in ? __ldg(prm.lse + grow) * LOG2E : INFINITY;
+    const float dsum = row_in ? __ldg(prm.dsum + grow) : 0.f;
+    bool ok = run;
+    for (int j = 0; j < NB && ok; ++j) {
+      int kp, kbk;
+      block_at(j, kp, kbk);
+      const int64_t kvalid = L - (int64_t)kbk * BM;
+      int hi = (int)min((int64_t)BM, kvalid);                                    // keys past the partition end
+      if (prm.causal && kp == p && kbk == qb) hi = min(hi, row + 1);             // diagonal block
+      const uint32_t tm_s = tmem + lane_base + (uint32_t)((j & 1) * 128);
+      ok = mbar_wait(bar(Ly::B_S + (j & 1)), (uint32_t)((j >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                     ROLE_EW, j);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float pv[BM];
+#pragma unroll
+      for (int c = 0; c < BM; c += 32) tmem_ld32(tm_s + (uint32_t)c, pv + c);
+      tc_wait_ld();
+      const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2);
+      const uint64_t nl2 = f2_pack(-lse2, -lse2);
+#pragma unroll
+      for (int c = 0; c < BM; c += 2) {
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), sc2, nl2), x0, x1);
+        pv[c] = (c < hi) ? fast_exp2(x0) : 0.f;
+        pv[c + 1] = (c + 1 < hi) ? fast_exp2(x1) : 0.f;
+      }
+      // the S buffer is free once read: tell the MMA issuer (it may compute S(j+2) into it)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Ly::B_P));
+      ok = mbar_wait(bar(Ly::B_DP), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, j);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t nd2 = f2_pack(-dsum, -dsum);
+#pragma unroll
+      for (int c0 = 0; c0 < BM; c0 += 64) {
+        float dp[64];
+        tmem_ld32(tm_dp + (uint32_t)c0, dp);
+        tmem_ld32(tm_dp + (uint32_t)c0 + 32u, dp + 32);
+        tc_wait_ld();
+        uint32_t ds2[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float a0, a1;
+          f2_unpack(f2_add(f2_pack(dp[c], dp[c + 1]), nd2), a0, a1);
+          ds2[c / 2] = pack_bf16x2(pv[c0 + c] * a0, pv[c0 + c + 1] * a1);
+        }
+        tmem_st32(tm_dp + (uint32_t)(c0 / 2), ds2);
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Ly::B_DS));
+    }
+    if (ok) {
+      ok = mbar_wait(bar(Ly::B_ACC), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, -1);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const int64_t prow = (((int64_t)b * prm.Hq + h) * prm.n_slots + it.slot) * L + q_local;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        float v[32];
+        tmem_ld32(tm_dq + (uint32_t)c, v);
+        tc_wait_ld();
+        if (row_in) {
+          float4* dst = reinterpret_cast<float4*>(prm.dq_part + prow * D + c);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(v[4 * e] * prm.scale, v[4 * e + 1] * prm.scale, v[4 * e + 2] * prm.scale,
+                                 v[4 * e + 3] * prm.scale);
+        }
+      }
+    }
+  } else if (warp == WARP_MMA) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t idesc_ss = idesc_bf16_f32(BM, BM, false);  // S = Q K^T, dP = dO V^T
+    constexpr uint32_t idesc_ts = idesc_bf16_f32(BM, D, true);    // dQ += dS K, K MN-major
+    const uint64_t qdesc = smem_desc_sw128(sb + Ly::RES0, 16u, 1024u);
+    const uint64_t gdesc = smem_desc_sw128(sb + Ly::RES1, 16u, 1024u);
+    constexpr uint64_t TILE16 = Ly::TILE >> 4;
+    const uint64_t str_kmaj = smem_desc_sw128(sb + Ly::STR0, 16u, 1024u);
+    const uint64_t str_mn = smem_desc_sw128(sb + Ly::STR0, Ly::BOX, 1024u);
+    // stage s: K at STR0 + 2 s TILE, V at STR0 + (2 s + 1) TILE
+    auto issue_s = [&](int s, int buf) {  // S = Q K^T into S buffer `buf`
+      const uint64_t kd = str_kmaj + (uint64_t)(2 * s) * TILE16;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        tc_mma_ss_warp(tmem + (uint32_t)(buf * 128), qdesc + kmaj_off<D>(kk), kd + kmaj_off<D>(kk), idesc_ss, kk > 0);
+      tc_commit_warp(bar(Ly::B_S + buf));
+    };
+    auto issue_dp = [&](int s) {  // dP = dO V^T
+      const uint64_t vd = str_kmaj + (uint64_t)(2 * s + 1) * TILE16;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        tc_mma_ss_warp(tmem + 256u, gdesc + kmaj_off<D>(kk), vd + kmaj_off<D>(kk), idesc_ss, kk > 0);
+      tc_commit_warp(bar(Ly::B_DP));
+    };
+    auto issue_dq = [&](int s, bool first) {  // dQ += dS K
+      const uint64_t kd = str_mn + (uint64_t)(2 * s) * TILE16;
+#pragma unroll
+      for (int kk = 0; kk < BM / 16; ++kk)
+        tc_mma_ts_warp(tmem + 384u, tmem + 256u + (uint32_t)(kk * 8), kd + (uint64_t)(kk * 128), idesc_ts,
+                       (!first || kk > 0) ? 1u : 0u);
+    };
+    bool ok = run && NB > 0;
+    if (ok) ok = mbar_wait_warp(bar(Ly::B_RES), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, -1);
+    if (ok) ok = mbar_wait_warp(bar(Ly::B_FULL), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, 0);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0, 0);
+      issue_dp(0);
+      if (NB > 1) {
+        ok = mbar_wait_warp(bar(Ly::B_FULL + 1), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, 1);
+        if (ok) {
+          tc_fence_after();
+          issue_s(1, 1);
+        }
+      }
+    }
+    for (int j = 0; j < NB && ok; ++j) {
+      const int s = j & 1;
+      // S(j) has been read (its buffer is free for S(j+2)) and dS(j) is in TMEM
+      ok = mbar_wait_warp(bar(Ly::B_P), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
+      if (ok)
+        ok = mbar_wait_warp(bar(Ly::B_DS), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
+      if (!ok) break;
+      tc_fence_after();
+      issue_dq(s, j == 0);
+      tc_commit_warp(bar(Ly::B_EMPTY + s));  // K(j) and V(j) are no longer read
+      if (j + 1 < NB) issue_dp((j + 1) & 1);  // V(j+1) landed with K(j+1), waited for above
+      if (j + 2 < NB) {
+        ok = mbar_wait_warp(bar(Ly::B_FULL + s), (uint32_t)(((j + 2) >> 1) & 1), prm.wait_limit_ns, abort_flag,
+                            prm.status, ROLE_MMA, j + 2);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(s, s);
+      }
+    }
+    if (ok) tc_commit_warp(bar(Ly::B_ACC));
+    tc_commit_warp(bar(Ly::B_DRAIN));
+    mbar_drain(bar(Ly::B_DRAIN), 0u, DRAIN_NS);
+  } else if (warp == WARP_LOAD && lane == 0) {
+    // ================================================================ producer
+    bool ok = run && NB > 0;
+    const int64_t qrow = ((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + (int64_t)qb * BM;
+    const int64_t kvbase = ((int64_t)b * prm.Hkv + hk) * prm.S;
+    int issued = 0;
+    if (ok) {
+      mbar_expect_tx(bar(Ly::B_RES), 2 * Ly::TILE);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_2d(sb + Ly::RES0 + (uint32_t)c * Ly::BOX, &tmQ, c * 64, (int32_t)qrow, bar(Ly::B_RES));
+        tma_load_2d(sb + Ly::RES1 + (uint32_t)c * Ly::BOX, &tmG, c * 64, (int32_t)qrow, bar(Ly::B_RES));
+      }
+    }
+    for (int j = 0; j < NB && ok; ++j) {
+      const int s = j & 1;
+      if (j >= 2) {
+        ok = mbar_wait(bar(Ly::B_EMPTY + s), (uint32_t)(((j >> 1) - 1) & 1), prm.wait_limit_ns, abort_flag,
+                       prm.status, ROLE_LOAD, j);
+        if (!ok) break;
+      }
+      int kp, kbk;
+      block_at(j, kp, kbk);
+      if (kp < 0 || kp >= prm.P) {
+        record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_LOAD, (int32_t)blockIdx.x);
+        *abort_flag = 1;
+        break;
+      }
+      const int32_t krow = (int32_t)(kvbase + (int64_t)kp * L + (int64_t)kbk * BM);
+      mbar_expect_tx(bar(Ly::B_FULL + s), 2 * Ly::TILE);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_2d(sb + Ly::STR0 + (uint32_t)(2 * s) * Ly::TILE + (uint32_t)c * Ly::BOX, &tmK, c * 64, krow,
+                    bar(Ly::B_FULL + s));
+        tma_load_2d(sb + Ly::STR0 + (uint32_t)(2 * s + 1) * Ly::TILE + (uint32_t)c * Ly::BOX, &tmV, c * 64, krow,
+                    bar(Ly::B_FULL + s));
+      }
+      ++issued;
+    }
+    if (run && NB > 0) mbar_drain(bar(Ly::B_RES), 0u, DRAIN_NS);
+    for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
+      mbar_drain(bar(Ly::B_FULL + (j & 1)), (uint32_t)((j >> 1) & 1), DRAIN_NS);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode(std::string* err) {
+  static EncodeTiledFn fn = nullptr;
+  if (fn) return fn;
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !ptr) {
+    *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return nullptr;
+  }
+  fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  return fn;
+}
+
+// [rows, d] bf16 row-major tensor, boxes of 128 rows x 64 columns with 128-byte swizzle.
+static bool make_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, uint64_t rows, int d, std::string* err) {
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)BM};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *err = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
+    return false;
+  }
+  return true;
+}
+
+template <int D>
+static int launch(const BwdArgs& a, void* stream, std::string* err) {
+  const int64_t nb = (a.L + BM - 1) / BM;
+  const int64_t dq_units = (int64_t)a.n_items * a.B * a.Hq * nb;
+  const int64_t kv_units = (int64_t)a.n_kv_items * a.B * a.Hkv * nb;
+  if (dq_units <= 0 && kv_units <= 0) return (int)cudaSuccess;
+  if (dq_units > 0x7fffffff || kv_units > 0x7fffffff) {
+    *err = "too many work units for one launch";
+    return (int)cudaErrorInvalidConfiguration;
+  }
+  EncodeTiledFn enc = get_encode(err);
+  if (!enc) return (int)cudaErrorNotSupported;
+  CUtensorMap mq, mk, mv, mg;
+  if (!make_map(enc, &mq, a.Q, (uint64_t)a.B * a.Hq * a.S, D, err) ||
+      !make_map(enc, &mk, a.K, (uint64_t)a.B * a.Hkv * a.S, D, err) ||
+      !make_map(enc, &mv, a.V, (uint64_t)a.B * a.Hkv * a.S, D, err) ||
+      !make_map(enc, &mg, a.dO, (uint64_t)a.B * a.Hq * a.S, D, err))
+    return (int)cudaErrorInvalidValue;
+  Params prm;
+  prm.items = a.items;
+  prm.kv_list = a.kv_list;
+  prm.kv_items = a.kv_items;
+  prm.q_list = a.q_list;
+  prm.lse = a.LSE;
+  prm.dsum = a.D;
+  prm.dq_part = a.dq_part;
+  prm.dk_part = a.dk_part;
+  prm.dv_part = a.dv_part;
+  prm.status = a.status;
+  prm.S = a.S;
+  prm.L = a.L;
+  prm.B = a.B;
+  prm.Hq = a.Hq;
+  prm.Hkv = a.Hkv;
+  prm.P = a.P;
+  prm.n_items = a.n_items;
+  prm.n_slots = a.n_slots;
+  prm.n_kv_items = a.n_kv_items;
+  prm.n_kv_slots = a.n_kv_slots;
+  prm.nb = (int32_t)nb;
+  prm.causal = a.causal;
+  prm.scale = a.scale;
+  prm.scale_log2 = a.scale_log2;
+  prm.wait_limit_ns = a.wait_limit_ns;
+  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)Layout<D>::ALLOC);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<D>::ALLOC);
+  if (e != cudaSuccess) {
+    *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+    return (int)e;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  if (kv_units > 0)
+    bwd_dkdv_kernel<D><<<dim3((unsigned)kv_units), dim3(NUM_THREADS), Layout<D>::ALLOC, st>>>(mq, mk, mv, mg, prm);
+  if (dq_units > 0)
+    bwd_dq_kernel<D><<<dim3((unsigned)dq_units), dim3(NUM_THREADS), Layout<D>::ALLOC, st>>>(mq, mk, mv, mg, prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) *err = std::string("tile_bwd_tc launch: ") + cudaGetErrorString(e);
+  return (int)e;
+}
+
+}  // namespace btc
+
+int launch_tile_bwd_tc(const BwdArgs& a, void* stream, std::string* err) {
+  if (a.d == 128) return btc::launch<128>(a, stream, err);
+  if (a.d == 64) return btc::launch<64>(a, stream, err);
+  *err = "tensor-core backward supports d = 64 or 128";
+  return (int)cudaErrorInvalidValue;
+}
+
 }  // namespace mesh
