@@ -23,7 +23,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from mesh_inputs import WORKLOADS, make_qkv, sample_rows  # noqa: E402
+from mesh_inputs import WORKLOADS, make_do, make_qkv, sample_rows  # noqa: E402
 
 METRIC = "mesh-tiled attention fwd TFLOP/s & % bf16 tensor peak; merge HBM GB/s (1 GB300)"
 UNIT = "TFLOP/s"
@@ -267,6 +267,64 @@ def run_e2e(m, w, args, q, k, v, dev, flops, world, barrier):
             "serial_value": job_throughput(world, flops, s_ms), "serial_ms_per_step": s_ms}
 
 
+def run_backward(m, w, plan, qd, kd, vd, O, LSE, dev, args, stream, flops):
+    """Time the backward pass (D = dO . O, tile backward, reduce) with CUDA events, inputs resident.
+
+    Algorithmic flops of the tile backward: the four gradient products dP = dO V^T, dV = P^T dO,
+    dQ = dS K, dK = dS^T Q over the visible pairs = 2x the forward's; the kernels also recompute
+    S (dK/dV kernel) and S, dP (dQ kernel): executed = 3.5x the forward's.
+    """
+    dO = make_do(w).to(dev)
+    dq_p, dk_p, dv_p = m.new_bwd_partials(plan, w.B, w.Hq, w.Hkv, w.d, dev)
+    wsb = m.new_bwd_workspace(plan, dev)
+    st = m.new_status(dev)
+    D = torch.empty(w.B, w.Hq, w.S, dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+
+    def bstep(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        m.mesh_attn_bwd_prep(O, dO, D, st, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        m.mesh_attn_tile_bwd(plan, qd, kd, vd, dO, LSE, D, None, dq_p, dk_p, dv_p, wsb, st, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        m.mesh_attn_bwd_reduce(plan, w.B, w.Hq, w.Hkv, w.d, dq_p, dk_p, dv_p, dQ, dK, dV, wsb, st, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        bstep()
+    steps = max(1, args.steps)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        bstep(evs[i])
+    torch.cuda.synchronize()
+    code = m.mesh_attn_read_status(st, stream)
+    if code != 0:
+        raise RuntimeError(f"device status {code} in the backward pass: {st.tolist()}")
+    prep_ms, tile_ms, red_ms = (sum(e[j].elapsed_time(e[j + 1]) for e in evs) / steps for j in range(3))
+    peaks, _ = load_peaks()
+    es = 2 if w.dtype == "bf16" else 4
+    alg = 2 * flops
+    tflops = alg / (tile_ms * 1e-3) / 1e12
+    nq, nkv = m.mesh_attn_bwd_partials_size(plan, w.B, w.Hq, w.Hkv, w.d)
+    red_bytes = 4.0 * (nq + 2 * nkv) + es * (w.B * w.Hq * w.S * w.d + 2 * w.B * w.Hkv * w.S * w.d)
+    prep_bytes = 2.0 * es * w.B * w.Hq * w.S * w.d + 4.0 * w.B * w.Hq * w.S
+    line = {"ms_per_step": prep_ms + tile_ms + red_ms, "steps": steps,
+            "tile_bwd_ms": tile_ms, "prep_ms": prep_ms, "reduce_ms": red_ms,
+            "flops_per_step": alg, "tflops": tflops, "unit": "TFLOP/s",
+            "executed_tflops": 3.5 * flops / (tile_ms * 1e-3) / 1e12,
+            "reduce_gbs": red_bytes / (red_ms * 1e-3) / 1e9, "prep_gbs": prep_bytes / (prep_ms * 1e-3) / 1e9}
+    if w.dtype == "bf16":
+        line["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": tflops / peaks["bf16_tflops"], "traffic": None,
+                            "kernel": "bwd_dkdv_kernel + bwd_dq_kernel"}
+    return line
+
+
 def workload_config(w, plan="mesh"):
     return {"workload": w.name, "plan": plan, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d, "in_dtype": w.dtype,
             "causal": w.causal, "P": w.P, "mesh": f"{w.R}x{w.R}", "kvr": w.kvr, "greedy": w.greedy,
@@ -284,6 +342,7 @@ def main():
                     help="tile assignment: sqrt(P) x sqrt(P) mesh with KVR (default) or Ring-Attention rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
@@ -362,6 +421,11 @@ def main():
     flops = algorithmic_flops(w)
     value = job_throughput(ws, flops, ms_per_step)
 
+    # backward pass on the same workload (a separate object of the line; not part of `value`)
+    bwd = None
+    if not args.no_backward:
+        bwd = run_backward(m, w, plan, qd, kd, vd, O, LSE, dev, args, stream, flops)
+
     # end to end through the public call, host buffers in pinned memory
     e2e = None
     if not args.no_e2e:
@@ -397,7 +461,7 @@ def main():
                      "kernel": "tile_fwd_tc_kernel", "peak_kind": f"{peak_kind} bf16 dense burst"},
         "merge": {"bound": "hbm", "achieved": merge_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                   "frac": merge_gbs / peaks["hbm_gbs"], "bytes_per_launch": mbytes, "ms": merge_ms},
-        "tile_fwd_ms": tile_ms, "merge_ms": merge_ms,
+        "tile_fwd_ms": tile_ms, "merge_ms": merge_ms, "backward": bwd,
         "comm_counted": counted_volumes(m, w),
         "cpu_baseline": cpu_base, "e2e": e2e, "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),

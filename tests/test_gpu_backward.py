@@ -184,3 +184,40 @@ def test_backward_bf16_plan_variants(lib):
         check_gradients(w, got, q, k, v, dO, tag=f" kvr={kvr} greedy={greedy}")
     got, _, _ = run_backward(lib, w, q, k, v, dO, plan=lib.mesh_attn_plan_create_ring(w.S, w.P, w.causal))
     check_gradients(w, got, q, k, v, dO, tag=" ring")
+
+
+@pytest.mark.parametrize("name", ["bf16_causal_16k", "gqa_causal_64k"])
+def test_backward_full_size(lib, name):
+    """Full-size workloads (the forward's bench configurations): dQ on seeded sampled rows against
+    the oracle one row at a time, and two identities that hold at any size for every KV head and
+    column: sum_j dK_j = scale sum_i q_i sum_j dS_ij = 0 and sum_j dV_j = sum_i dO_i (rows of P sum
+    to 1), each within 2^-7 of the sum of the terms' magnitudes."""
+    import numpy as np
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w)
+    dO = make_do(w)
+    got, plan, _ = run_backward(lib, w, q, k, v, dO)
+    dQ, dK, dV = (t.double().cpu() for t in got[:3])
+    del got
+    g = w.Hq // w.Hkv
+    dk_sum = dK.sum(dim=2)
+    dk_abs = dK.abs().sum(dim=2)
+    assert (dk_sum.abs() <= 2.0 ** -7 * dk_abs + 1e-3).all(), (dk_sum.abs() / dk_abs).max().item()
+    dv_sum = dV.sum(dim=2)
+    want = dO.double().view(w.B, w.Hkv, g, w.S, w.d).sum(dim=(2, 3))
+    dv_abs = dV.abs().sum(dim=2)
+    assert ((dv_sum - want).abs() <= 2.0 ** -7 * dv_abs + 1e-3).all()
+    rng = np.random.default_rng(w.cfg_id)
+    rows = np.stack([np.stack([np.sort(rng.choice(w.S, 24, replace=False)) for _ in range(w.Hq)])
+                     for _ in range(w.B)])
+    rows[..., 0] = 0
+    rows[..., -1] = w.S - 1
+    ref = OB.dq_rows(q, k, v, dO, w.causal, rows)
+    got_rows = torch.stack([torch.stack([dQ[b, h, torch.as_tensor(rows[b, h])] for h in range(w.Hq)])
+                            for b in range(w.B)])
+    e = (got_rows - ref).abs()
+    # the rows' magnitude bound would need the full forward; use 2^-7 of the row's largest value
+    bound = 2.0 ** -7 * ref.abs().amax(dim=-1, keepdim=True) + 2e-3
+    print(f"[parity-bwd] {name} sampled dQ rows: max|err| = {e.max().item():.3e}, "
+          f"max err/bound = {(e / bound).max().item():.3f}")
+    assert (e <= bound).all()

@@ -57,3 +57,36 @@ def test_empty_and_degenerate_launches(lib):
     lib.mesh_attn_tile_fwd(plan, q, q[:, :1], q[:, :1], None, po, pl, ws, st)
     lib.mesh_attn_merge(plan, 1, 2, 128, po, pl, O, LSE, ws, st)
     assert lib.mesh_attn_read_status(st) == 0
+
+
+def test_backward_wait_timeout_reports_status_and_context_survives(lib):
+    """The tensor-core backward kernels under a zero wait limit: status DEVICE_TIMEOUT, the reduce
+    skips its work, and after a reset the same context produces correct gradients."""
+    from mesh_inputs import make_do
+    from tests.test_gpu_backward import check_gradients
+    w = Workload(121, "status_bwd", 1, 2, 1, 2048, 128, "bf16", True, 4)
+    q, k, v = make_qkv(w)
+    dO = make_do(w)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
+    plan = lib.mesh_attn_plan_create(w.S, w.P, w.causal, True, True)
+    O, LSE = lib.mesh_attention(qd, kd, vd, w.P, w.causal, plan=plan)
+    dq_p, dk_p, dv_p = lib.new_bwd_partials(plan, 1, 2, 1, 128)
+    ws = lib.new_bwd_workspace(plan)
+    st = lib.new_status()
+    D = torch.empty(1, 2, w.S, device="cuda")
+    dQ, dK, dV = (torch.full_like(t, 7.0) for t in (qd, kd, vd))
+    lib.mesh_attn_bwd_prep(O, dod, D, st)
+    lib.mesh_attn_set_wait_limit_ns(0)
+    try:
+        lib.mesh_attn_tile_bwd(plan, qd, kd, vd, dod, LSE, D, None, dq_p, dk_p, dv_p, ws, st)
+        code = lib.mesh_attn_read_status(st)
+    finally:
+        lib.mesh_attn_set_wait_limit_ns(2_000_000_000)
+    assert code == 5, f"status block {st.tolist()}"
+    assert st[1].item() in (1, 2, 3)
+    lib.mesh_attn_bwd_reduce(plan, 1, 2, 1, 128, dq_p, dk_p, dv_p, dQ, dK, dV, ws, st)
+    assert lib.mesh_attn_read_status(st) == 5
+    assert bool((dQ == 7.0).all()) and bool((dK == 7.0).all()) and bool((dV == 7.0).all())
+    st.zero_()
+    got = lib.mesh_attention_backward(qd, kd, vd, O, LSE, dod, w.P, w.causal, plan=plan)
+    check_gradients(w, got, q, k, v, dO)
