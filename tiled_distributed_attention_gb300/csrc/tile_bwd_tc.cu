@@ -13,7 +13,8 @@
 //   warp 5     producer: TMA loads of 128 x 64 bf16 boxes with 128-byte swizzle
 //
 // dkdv (unit = KV slot, batch, KV head, 128-key block): K and V stay in shared memory; Q and dO
-// blocks of the slot's query rows (over the KV head's query heads) stream through two stages.
+// blocks of the slot's query rows (over the KV head's query heads) stream through three and two
+// stages (Q feeds S^T one block ahead of its last use).
 //   TMEM: S^T | dP^T | dV | dK   (S^T = K Q^T and dP^T = V dO^T have lanes = keys; P^T and dS^T
 //   are written back as bf16 into the first half of their columns and feed dV += P^T dO and
 //   dK += dS^T Q from TMEM).  Issue order per query block i:
@@ -22,7 +23,7 @@
 //   dV(i+1) and S^T(i+2).  LSE and D of the block's query columns are broadcast from shared
 //   memory.
 // dq (unit = forward work item, batch, head, 128-row block): Q and dO stay in shared memory; K
-//   and V blocks of the item's KV partitions stream through two stages.
+//   and V blocks of the item's KV partitions stream through three and two stages.
 //   TMEM: S(even) | S(odd) | dP | dQ: S(j+2) is issued as soon as its K block has landed, so
 //   the exponentials of block j+1 run while dQ(j) and dP(j+1) execute.  LSE and D of a row are
 //   thread-local.
@@ -64,19 +65,27 @@ struct Params {
   int64_t wait_limit_ns;
 };
 
+// Shared memory: the resident pair (K, V in dkdv; Q, dO in dq), NSA stages of stream A (the
+// operand of the S product, needed two blocks ahead: Q in dkdv, K in dq) and NSB stages of
+// stream B (dO in dkdv, V in dq).  224 KB for d = 128 leaves no room to align the base by hand:
+// the kernels check that the dynamic shared window starts 1024-aligned (it does on sm_100-class
+// parts, whose window starts at a 1 KB-aligned offset) and report MESH_ATTN_ERR_INTERNAL if not.
 template <int D>
 struct Layout {
   static constexpr uint32_t TILE = BM * D * 2;  // one 128-row bf16 block
   static constexpr uint32_t BOX = BM * 64 * 2;  // one 128 x 64 TMA box
-  // resident pair (K, V in dkdv; Q, dO in dq), then two stages of the streamed pair
-  static constexpr uint32_t RES0 = 0, RES1 = TILE, STR0 = 2 * TILE;  // stage s: STR0 + s*2*TILE (+TILE)
-  static constexpr uint32_t VEC_OFF = STR0 + 4 * TILE;  // dkdv: lse2[2][128], dsum[2][128] fp32
+  static constexpr int NSA = 3, NSB = 2;
+  static constexpr uint32_t RES0 = 0, RES1 = TILE;
+  static constexpr uint32_t A0 = 2 * TILE;             // stream A stage s at A0 + s TILE
+  static constexpr uint32_t B0 = A0 + NSA * TILE;      // stream B stage s at B0 + s TILE
+  static constexpr uint32_t VEC_OFF = B0 + NSB * TILE;  // dkdv: lse2[2][128], dsum[2][128] fp32
   static constexpr uint32_t BAR_OFF = VEC_OFF + 4 * BM * 4;
-  static constexpr int B_RES = 0, B_FULL = 1, B_EMPTY = 3, B_S = 5, B_DP = 7, B_P = 8, B_DS = 9, B_ACC = 10,
-                       B_DRAIN = 11, B_VEC = 12, NBARS = 14;
+  static constexpr int B_RES = 0, B_AF = 1, B_AE = B_AF + NSA, B_BF = B_AE + NSA, B_BE = B_BF + NSB,
+                       B_S = B_BE + NSB, B_DP = B_S + 2, B_P = B_DP + 1, B_DS = B_P + 1, B_ACC = B_DS + 1,
+                       B_DRAIN = B_ACC + 1, B_VEC = B_DRAIN + 1, NBARS = B_VEC + 2;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag
   static constexpr uint32_t TOTAL = MISC_OFF + 16;
-  static constexpr uint32_t ALLOC = TOTAL + 1024;
+  static constexpr uint32_t ALLOC = TOTAL;
 };
 
 // 128-row blocks of partition `k` (keys, dq kernel) visited by query block `qb` of partition
@@ -101,9 +110,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const Params prm) {
   using Ly = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sb = (raw + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (sb - raw);
+  const uint32_t sb = smem_u32(smem_raw);
+  if (sb & 1023u) {  // 128-byte swizzle atoms need 1024-aligned operands (see Layout)
+    if (threadIdx.x == 0) record_error(prm.status, MESH_ATTN_ERR_INTERNAL, ROLE_ITEM, (int32_t)blockIdx.x);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) { return sb + Ly::BAR_OFF + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::MISC_OFF);
@@ -134,9 +146,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Ly::B_RES), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(Ly::B_FULL + s), 1);
-      mbar_init(bar(Ly::B_EMPTY + s), 1);
+    for (int s = 0; s < Ly::NSA; ++s) {
+      mbar_init(bar(Ly::B_AF + s), 1);
+      mbar_init(bar(Ly::B_AE + s), 1);
+    }
+    for (int s = 0; s < Ly::NSB; ++s) {
+      mbar_init(bar(Ly::B_BF + s), 1);
+      mbar_init(bar(Ly::B_BE + s), 1);
     }
     mbar_init(bar(Ly::B_S), 1);
     mbar_init(bar(Ly::B_S + 1), 1);
@@ -325,64 +341,77 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint64_t kdesc = smem_desc_sw128(sb + Ly::RES0, 16u, 1024u);
     const uint64_t vdesc = smem_desc_sw128(sb + Ly::RES1, 16u, 1024u);
     constexpr uint64_t TILE16 = Ly::TILE >> 4;
-    const uint64_t str_kmaj = smem_desc_sw128(sb + Ly::STR0, 16u, 1024u);
-    const uint64_t str_mn = smem_desc_sw128(sb + Ly::STR0, Ly::BOX, 1024u);
-    // stage s: Q at STR0 + 2 s TILE, dO at STR0 + (2 s + 1) TILE
-    auto issue_s = [&](int s) {  // S^T = K Q^T
-      const uint64_t qd = str_kmaj + (uint64_t)(2 * s) * TILE16;
+    const uint64_t a_kmaj = smem_desc_sw128(sb + Ly::A0, 16u, 1024u);   // Q stages
+    const uint64_t a_mn = smem_desc_sw128(sb + Ly::A0, Ly::BOX, 1024u);
+    const uint64_t b_kmaj = smem_desc_sw128(sb + Ly::B0, 16u, 1024u);   // dO stages
+    const uint64_t b_mn = smem_desc_sw128(sb + Ly::B0, Ly::BOX, 1024u);
+    auto issue_s = [&](int sa) {  // S^T = K Q^T
+      const uint64_t qd = a_kmaj + (uint64_t)sa * TILE16;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         tc_mma_ss_warp(tmem, kdesc + kmaj_off<D>(kk), qd + kmaj_off<D>(kk), idesc_ss, kk > 0);
       tc_commit_warp(bar(Ly::B_S));
     };
-    auto issue_dp = [&](int s) {  // dP^T = V dO^T
-      const uint64_t gd = str_kmaj + (uint64_t)(2 * s + 1) * TILE16;
+    auto issue_dp = [&](int sbb) {  // dP^T = V dO^T
+      const uint64_t gd = b_kmaj + (uint64_t)sbb * TILE16;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         tc_mma_ss_warp(tmem + 128u, vdesc + kmaj_off<D>(kk), gd + kmaj_off<D>(kk), idesc_ss, kk > 0);
       tc_commit_warp(bar(Ly::B_DP));
     };
-    auto issue_dv = [&](int s, bool first) {  // dV += P^T dO
-      const uint64_t gd = str_mn + (uint64_t)(2 * s + 1) * TILE16;
+    auto issue_dv = [&](int sbb, bool first) {  // dV += P^T dO
+      const uint64_t gd = b_mn + (uint64_t)sbb * TILE16;
 #pragma unroll
       for (int kk = 0; kk < BM / 16; ++kk)
         tc_mma_ts_warp(tmem + 256u, tmem + (uint32_t)(kk * 8), gd + (uint64_t)(kk * 128), idesc_ts,
                        (!first || kk > 0) ? 1u : 0u);
     };
-    auto issue_dk = [&](int s, bool first) {  // dK += dS^T Q
-      const uint64_t qd = str_mn + (uint64_t)(2 * s) * TILE16;
+    auto issue_dk = [&](int sa, bool first) {  // dK += dS^T Q
+      const uint64_t qd = a_mn + (uint64_t)sa * TILE16;
 #pragma unroll
       for (int kk = 0; kk < BM / 16; ++kk)
         tc_mma_ts_warp(tmem + 256u + (uint32_t)D, tmem + 128u + (uint32_t)(kk * 8), qd + (uint64_t)(kk * 128),
                        idesc_ts, (!first || kk > 0) ? 1u : 0u);
     };
+    auto wait_a = [&](int i) {  // Q(i) landed
+      return mbar_wait_warp(bar(Ly::B_AF + i % Ly::NSA), (uint32_t)((i / Ly::NSA) & 1), prm.wait_limit_ns, abort_flag,
+                            prm.status, ROLE_MMA, i);
+    };
+    auto wait_b = [&](int i) {  // dO(i) landed
+      return mbar_wait_warp(bar(Ly::B_BF + i % Ly::NSB), (uint32_t)((i / Ly::NSB) & 1), prm.wait_limit_ns, abort_flag,
+                            prm.status, ROLE_MMA, i);
+    };
     bool ok = run && NBQ > 0;
     if (ok) ok = mbar_wait_warp(bar(Ly::B_RES), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, -1);
-    if (ok) ok = mbar_wait_warp(bar(Ly::B_FULL), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, 0);
+    if (ok) ok = wait_a(0) && wait_b(0);
     if (ok) {
       tc_fence_after();
       issue_s(0);
       issue_dp(0);
     }
     for (int i = 0; i < NBQ && ok; ++i) {
-      const int s = i & 1, sn = (i + 1) & 1;
       ok = mbar_wait_warp(bar(Ly::B_P), (uint32_t)(i & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, i);
       if (!ok) break;
       tc_fence_after();
-      issue_dv(s, i == 0);
+      issue_dv(i % Ly::NSB, i == 0);
+      tc_commit_warp(bar(Ly::B_BE + i % Ly::NSB));  // dO(i): read by dP^T(i) and dV(i)
       if (i + 1 < NBQ) {
-        ok = mbar_wait_warp(bar(Ly::B_FULL + sn), (uint32_t)(((i + 1) >> 1) & 1), prm.wait_limit_ns, abort_flag,
-                            prm.status, ROLE_MMA, i + 1);
+        ok = wait_a(i + 1);
         if (!ok) break;
         tc_fence_after();
-        issue_s(sn);
+        issue_s((i + 1) % Ly::NSA);
       }
       ok = mbar_wait_warp(bar(Ly::B_DS), (uint32_t)(i & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, i);
       if (!ok) break;
       tc_fence_after();
-      issue_dk(s, i == 0);
-      tc_commit_warp(bar(Ly::B_EMPTY + s));  // Q(i) and dO(i) are no longer read
-      if (i + 1 < NBQ) issue_dp(sn);
+      issue_dk(i % Ly::NSA, i == 0);
+      tc_commit_warp(bar(Ly::B_AE + i % Ly::NSA));  // Q(i): read by S^T(i) and dK(i)
+      if (i + 1 < NBQ) {
+        ok = wait_b(i + 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_dp((i + 1) % Ly::NSB);
+      }
     }
     if (ok) tc_commit_warp(bar(Ly::B_ACC));
     tc_commit_warp(bar(Ly::B_DRAIN));
@@ -391,7 +420,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ================================================================ producer
     bool ok = run && NBQ > 0;
     const int64_t kvrow = ((int64_t)b * prm.Hkv + hk) * prm.S + (int64_t)k * L + (int64_t)kb * BM;
-    int issued = 0;
     if (ok) {
       mbar_expect_tx(bar(Ly::B_RES), 2 * Ly::TILE);
       for (int c = 0; c < D / 64; ++c) {
@@ -399,13 +427,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_load_2d(sb + Ly::RES1 + (uint32_t)c * Ly::BOX, &tmV, c * 64, (int32_t)kvrow, bar(Ly::B_RES));
       }
     }
+    int issued_a = 0, issued_b = 0;
     for (int i = 0; i < NBQ && ok; ++i) {
-      const int s = i & 1;
-      if (i >= 2) {
-        ok = mbar_wait(bar(Ly::B_EMPTY + s), (uint32_t)(((i >> 1) - 1) & 1), prm.wait_limit_ns, abort_flag,
-                       prm.status, ROLE_LOAD, i);
-        if (!ok) break;
-      }
       int h, p, qb;
       block_at(i, h, p, qb);
       if (p < 0 || p >= prm.P) {
@@ -414,19 +437,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       const int32_t qrow = (int32_t)(((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + (int64_t)qb * BM);
-      mbar_expect_tx(bar(Ly::B_FULL + s), 2 * Ly::TILE);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_2d(sb + Ly::STR0 + (uint32_t)(2 * s) * Ly::TILE + (uint32_t)c * Ly::BOX, &tmQ, c * 64, qrow,
-                    bar(Ly::B_FULL + s));
-        tma_load_2d(sb + Ly::STR0 + (uint32_t)(2 * s + 1) * Ly::TILE + (uint32_t)c * Ly::BOX, &tmG, c * 64, qrow,
-                    bar(Ly::B_FULL + s));
+      const int sa = i % Ly::NSA, sbb = i % Ly::NSB;
+      if (i >= Ly::NSA) {
+        ok = mbar_wait(bar(Ly::B_AE + sa), (uint32_t)((i / Ly::NSA - 1) & 1), prm.wait_limit_ns, abort_flag,
+                       prm.status, ROLE_LOAD, i);
+        if (!ok) break;
       }
-      ++issued;
+      mbar_expect_tx(bar(Ly::B_AF + sa), Ly::TILE);
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_2d(sb + Ly::A0 + (uint32_t)sa * Ly::TILE + (uint32_t)c * Ly::BOX, &tmQ, c * 64, qrow,
+                    bar(Ly::B_AF + sa));
+      ++issued_a;
+      if (i >= Ly::NSB) {
+        ok = mbar_wait(bar(Ly::B_BE + sbb), (uint32_t)((i / Ly::NSB - 1) & 1), prm.wait_limit_ns, abort_flag,
+                       prm.status, ROLE_LOAD, i);
+        if (!ok) break;
+      }
+      mbar_expect_tx(bar(Ly::B_BF + sbb), Ly::TILE);
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_2d(sb + Ly::B0 + (uint32_t)sbb * Ly::TILE + (uint32_t)c * Ly::BOX, &tmG, c * 64, qrow,
+                    bar(Ly::B_BF + sbb));
+      ++issued_b;
     }
     // exit-path drain: every load issued lands before the CTA exits
     if (run && NBQ > 0) mbar_drain(bar(Ly::B_RES), 0u, DRAIN_NS);
-    for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
-      mbar_drain(bar(Ly::B_FULL + (j & 1)), (uint32_t)((j >> 1) & 1), DRAIN_NS);
+    for (int j = (issued_a > Ly::NSA ? issued_a - Ly::NSA : 0); j < issued_a; ++j)
+      mbar_drain(bar(Ly::B_AF + j % Ly::NSA), (uint32_t)((j / Ly::NSA) & 1), DRAIN_NS);
+    for (int j = (issued_b > Ly::NSB ? issued_b - Ly::NSB : 0); j < issued_b; ++j)
+      mbar_drain(bar(Ly::B_BF + j % Ly::NSB), (uint32_t)((j / Ly::NSB) & 1), DRAIN_NS);
   }
 
   tc_fence_before();
@@ -445,9 +483,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   const Params prm) {
   using Ly = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sb = (raw + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (sb - raw);
+  const uint32_t sb = smem_u32(smem_raw);
+  if (sb & 1023u) {  // 128-byte swizzle atoms need 1024-aligned operands (see Layout)
+    if (threadIdx.x == 0) record_error(prm.status, MESH_ATTN_ERR_INTERNAL, ROLE_ITEM, (int32_t)blockIdx.x);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) { return sb + Ly::BAR_OFF + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::MISC_OFF);
@@ -471,11 +512,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Ly::B_RES), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(Ly::B_FULL + s), 1);
-      mbar_init(bar(Ly::B_EMPTY + s), 1);
-      mbar_init(bar(Ly::B_S + s), 1);
+    for (int s = 0; s < Ly::NSA; ++s) {
+      mbar_init(bar(Ly::B_AF + s), 1);
+      mbar_init(bar(Ly::B_AE + s), 1);
     }
+    for (int s = 0; s < Ly::NSB; ++s) {
+      mbar_init(bar(Ly::B_BF + s), 1);
+      mbar_init(bar(Ly::B_BE + s), 1);
+    }
+    mbar_init(bar(Ly::B_S), 1);
+    mbar_init(bar(Ly::B_S + 1), 1);
     mbar_init(bar(Ly::B_DP), 1);
     mbar_init(bar(Ly::B_P), 4);
     mbar_init(bar(Ly::B_DS), 4);
@@ -612,39 +658,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint64_t qdesc = smem_desc_sw128(sb + Ly::RES0, 16u, 1024u);
     const uint64_t gdesc = smem_desc_sw128(sb + Ly::RES1, 16u, 1024u);
     constexpr uint64_t TILE16 = Ly::TILE >> 4;
-    const uint64_t str_kmaj = smem_desc_sw128(sb + Ly::STR0, 16u, 1024u);
-    const uint64_t str_mn = smem_desc_sw128(sb + Ly::STR0, Ly::BOX, 1024u);
-    // stage s: K at STR0 + 2 s TILE, V at STR0 + (2 s + 1) TILE
-    auto issue_s = [&](int s, int buf) {  // S = Q K^T into S buffer `buf`
-      const uint64_t kd = str_kmaj + (uint64_t)(2 * s) * TILE16;
+    const uint64_t a_kmaj = smem_desc_sw128(sb + Ly::A0, 16u, 1024u);  // K stages
+    const uint64_t a_mn = smem_desc_sw128(sb + Ly::A0, Ly::BOX, 1024u);
+    const uint64_t b_kmaj = smem_desc_sw128(sb + Ly::B0, 16u, 1024u);  // V stages
+    auto issue_s = [&](int sa, int buf) {  // S = Q K^T into S buffer `buf`
+      const uint64_t kd = a_kmaj + (uint64_t)sa * TILE16;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         tc_mma_ss_warp(tmem + (uint32_t)(buf * 128), qdesc + kmaj_off<D>(kk), kd + kmaj_off<D>(kk), idesc_ss, kk > 0);
       tc_commit_warp(bar(Ly::B_S + buf));
     };
-    auto issue_dp = [&](int s) {  // dP = dO V^T
-      const uint64_t vd = str_kmaj + (uint64_t)(2 * s + 1) * TILE16;
+    auto issue_dp = [&](int sbb) {  // dP = dO V^T; V(j) is read by this product only
+      const uint64_t vd = b_kmaj + (uint64_t)sbb * TILE16;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         tc_mma_ss_warp(tmem + 256u, gdesc + kmaj_off<D>(kk), vd + kmaj_off<D>(kk), idesc_ss, kk > 0);
       tc_commit_warp(bar(Ly::B_DP));
+      tc_commit_warp(bar(Ly::B_BE + sbb));
     };
-    auto issue_dq = [&](int s, bool first) {  // dQ += dS K
-      const uint64_t kd = str_mn + (uint64_t)(2 * s) * TILE16;
+    auto issue_dq = [&](int sa, bool first) {  // dQ += dS K
+      const uint64_t kd = a_mn + (uint64_t)sa * TILE16;
 #pragma unroll
       for (int kk = 0; kk < BM / 16; ++kk)
         tc_mma_ts_warp(tmem + 384u, tmem + 256u + (uint32_t)(kk * 8), kd + (uint64_t)(kk * 128), idesc_ts,
                        (!first || kk > 0) ? 1u : 0u);
     };
+    auto wait_a = [&](int j) {  // K(j) landed
+      return mbar_wait_warp(bar(Ly::B_AF + j % Ly::NSA), (uint32_t)((j / Ly::NSA) & 1), prm.wait_limit_ns, abort_flag,
+                            prm.status, ROLE_MMA, j);
+    };
+    auto wait_b = [&](int j) {  // V(j) landed
+      return mbar_wait_warp(bar(Ly::B_BF + j % Ly::NSB), (uint32_t)((j / Ly::NSB) & 1), prm.wait_limit_ns, abort_flag,
+                            prm.status, ROLE_MMA, j);
+    };
     bool ok = run && NB > 0;
     if (ok) ok = mbar_wait_warp(bar(Ly::B_RES), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, -1);
-    if (ok) ok = mbar_wait_warp(bar(Ly::B_FULL), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, 0);
+    if (ok) ok = wait_a(0);
     if (ok) {
       tc_fence_after();
       issue_s(0, 0);
+      ok = wait_b(0);
+    }
+    if (ok) {
+      tc_fence_after();
       issue_dp(0);
       if (NB > 1) {
-        ok = mbar_wait_warp(bar(Ly::B_FULL + 1), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, 1);
+        ok = wait_a(1);
         if (ok) {
           tc_fence_after();
           issue_s(1, 1);
@@ -652,22 +711,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     for (int j = 0; j < NB && ok; ++j) {
-      const int s = j & 1;
       // S(j) has been read (its buffer is free for S(j+2)) and dS(j) is in TMEM
       ok = mbar_wait_warp(bar(Ly::B_P), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
       if (ok)
         ok = mbar_wait_warp(bar(Ly::B_DS), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
       if (!ok) break;
       tc_fence_after();
-      issue_dq(s, j == 0);
-      tc_commit_warp(bar(Ly::B_EMPTY + s));  // K(j) and V(j) are no longer read
-      if (j + 1 < NB) issue_dp((j + 1) & 1);  // V(j+1) landed with K(j+1), waited for above
-      if (j + 2 < NB) {
-        ok = mbar_wait_warp(bar(Ly::B_FULL + s), (uint32_t)(((j + 2) >> 1) & 1), prm.wait_limit_ns, abort_flag,
-                            prm.status, ROLE_MMA, j + 2);
+      issue_dq(j % Ly::NSA, j == 0);
+      tc_commit_warp(bar(Ly::B_AE + j % Ly::NSA));  // K(j): read by S(j) and dQ(j)
+      if (j + 1 < NB) {
+        ok = wait_b(j + 1);
         if (!ok) break;
         tc_fence_after();
-        issue_s(s, s);
+        issue_dp((j + 1) % Ly::NSB);
+      }
+      if (j + 2 < NB) {
+        ok = wait_a(j + 2);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s((j + 2) % Ly::NSA, j & 1);
       }
     }
     if (ok) tc_commit_warp(bar(Ly::B_ACC));
@@ -678,7 +740,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = run && NB > 0;
     const int64_t qrow = ((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + (int64_t)qb * BM;
     const int64_t kvbase = ((int64_t)b * prm.Hkv + hk) * prm.S;
-    int issued = 0;
     if (ok) {
       mbar_expect_tx(bar(Ly::B_RES), 2 * Ly::TILE);
       for (int c = 0; c < D / 64; ++c) {
@@ -686,13 +747,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_load_2d(sb + Ly::RES1 + (uint32_t)c * Ly::BOX, &tmG, c * 64, (int32_t)qrow, bar(Ly::B_RES));
       }
     }
+    int issued_a = 0, issued_b = 0;
     for (int j = 0; j < NB && ok; ++j) {
-      const int s = j & 1;
-      if (j >= 2) {
-        ok = mbar_wait(bar(Ly::B_EMPTY + s), (uint32_t)(((j >> 1) - 1) & 1), prm.wait_limit_ns, abort_flag,
-                       prm.status, ROLE_LOAD, j);
-        if (!ok) break;
-      }
       int kp, kbk;
       block_at(j, kp, kbk);
       if (kp < 0 || kp >= prm.P) {
@@ -701,18 +757,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       const int32_t krow = (int32_t)(kvbase + (int64_t)kp * L + (int64_t)kbk * BM);
-      mbar_expect_tx(bar(Ly::B_FULL + s), 2 * Ly::TILE);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_2d(sb + Ly::STR0 + (uint32_t)(2 * s) * Ly::TILE + (uint32_t)c * Ly::BOX, &tmK, c * 64, krow,
-                    bar(Ly::B_FULL + s));
-        tma_load_2d(sb + Ly::STR0 + (uint32_t)(2 * s + 1) * Ly::TILE + (uint32_t)c * Ly::BOX, &tmV, c * 64, krow,
-                    bar(Ly::B_FULL + s));
+      const int sa = j % Ly::NSA, sbb = j % Ly::NSB;
+      if (j >= Ly::NSA) {
+        ok = mbar_wait(bar(Ly::B_AE + sa), (uint32_t)((j / Ly::NSA - 1) & 1), prm.wait_limit_ns, abort_flag,
+                       prm.status, ROLE_LOAD, j);
+        if (!ok) break;
       }
-      ++issued;
+      mbar_expect_tx(bar(Ly::B_AF + sa), Ly::TILE);
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_2d(sb + Ly::A0 + (uint32_t)sa * Ly::TILE + (uint32_t)c * Ly::BOX, &tmK, c * 64, krow,
+                    bar(Ly::B_AF + sa));
+      ++issued_a;
+      if (j >= Ly::NSB) {
+        ok = mbar_wait(bar(Ly::B_BE + sbb), (uint32_t)((j / Ly::NSB - 1) & 1), prm.wait_limit_ns, abort_flag,
+                       prm.status, ROLE_LOAD, j);
+        if (!ok) break;
+      }
+      mbar_expect_tx(bar(Ly::B_BF + sbb), Ly::TILE);
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_2d(sb + Ly::B0 + (uint32_t)sbb * Ly::TILE + (uint32_t)c * Ly::BOX, &tmV, c * 64, krow,
+                    bar(Ly::B_BF + sbb));
+      ++issued_b;
     }
     if (run && NB > 0) mbar_drain(bar(Ly::B_RES), 0u, DRAIN_NS);
-    for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
-      mbar_drain(bar(Ly::B_FULL + (j & 1)), (uint32_t)((j >> 1) & 1), DRAIN_NS);
+    for (int j = (issued_a > Ly::NSA ? issued_a - Ly::NSA : 0); j < issued_a; ++j)
+      mbar_drain(bar(Ly::B_AF + j % Ly::NSA), (uint32_t)((j / Ly::NSA) & 1), DRAIN_NS);
+    for (int j = (issued_b > Ly::NSB ? issued_b - Ly::NSB : 0); j < issued_b; ++j)
+      mbar_drain(bar(Ly::B_BF + j % Ly::NSB), (uint32_t)((j / Ly::NSB) & 1), DRAIN_NS);
   }
 
   tc_fence_before();
