@@ -120,8 +120,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto bar = [&](int i) { return sb + Ly::BAR_OFF + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::MISC_OFF);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + Ly::MISC_OFF + 4);
-  float* lse_s = reinterpret_cast<float*>(smem + Ly::VEC_OFF);  // [2][BM] LSE * log2 e
-  float* dsum_s = lse_s + 2 * BM;                               // [2][BM]
+  float* nlse_s = reinterpret_cast<float*>(smem + Ly::VEC_OFF);  // [2][BM] -LSE log2 e of the query columns
+  float* ndsum_s = nlse_s + 2 * BM;                              // [2][BM] -D
   const int64_t L = prm.L;
 
   // unit -> (KV slot, batch, KV head, key block)
@@ -220,10 +220,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int64_t ql = (int64_t)qb * BM + row;
       if (p >= 0 && p < prm.P && ql < L) {
         const int64_t gi = ((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + ql;
-        nxt_lse = __ldg(prm.lse + gi) * LOG2E;
-        nxt_d = __ldg(prm.dsum + gi);
+        nxt_lse = -__ldg(prm.lse + gi) * LOG2E;
+        nxt_d = -__ldg(prm.dsum + gi);
       } else {
-        nxt_lse = INFINITY;  // no row: exp2(s - inf) = 0
+        nxt_lse = -INFINITY;  // no such query row: exp2(s - inf) = 0, so it needs no mask
         nxt_d = 0.f;
       }
     };
@@ -232,8 +232,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int vb = i & 1;
       // publish this row's LSE / D, then wait (bounded) until all 128 columns are written; a
       // buffer is rewritten two blocks later, after every thread has arrived for the block between
-      lse_s[vb * BM + row] = nxt_lse;
-      dsum_s[vb * BM + row] = nxt_d;
+      nlse_s[vb * BM + row] = nxt_lse;
+      ndsum_s[vb * BM + row] = nxt_d;
       mbar_arrive(bar(Ly::B_VEC + vb));
       if (i + 1 < NBQ) fetch(i + 1);
       ok = mbar_wait(bar(Ly::B_VEC + vb), (uint32_t)((i >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
@@ -243,9 +243,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int h, p, qb;
       block_at(i, h, p, qb);
       (void)h;
-      // visible query columns of this key row: [lo, hi)
-      const int64_t qvalid = L - (int64_t)qb * BM;
-      const int hi = (int)min((int64_t)BM, qvalid);
+      // causal diagonal block: query columns before this key row are masked (query rows past the
+      // partition end carry -inf in place of -LSE and need no mask)
       const int lo = (prm.causal && p == k && qb == kb) ? row : 0;
       ok = mbar_wait(bar(Ly::B_S), (uint32_t)(i & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, i);
       ok = __all_sync(0xffffffffu, ok);
@@ -255,24 +254,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
       for (int c = 0; c < BM; c += 32) tmem_ld32(tm_s + (uint32_t)c, pv + c);
       tc_wait_ld();
-      const float* lv = lse_s + vb * BM;
-      const bool full = (lo == 0 && hi == BM) || key_local >= L;
+      if (__any_sync(0xffffffffu, lo > 0)) {
+#pragma unroll
+        for (int c = 0; c < BM; ++c)
+          if (c < lo) pv[c] = -INFINITY;
+      }
+      const float4* lv = reinterpret_cast<const float4*>(nlse_s + vb * BM);
+      const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2);
       uint32_t pk[BM / 2];
 #pragma unroll
-      for (int c = 0; c < BM; c += 2) {
-        const float2 l2 = *reinterpret_cast<const float2*>(lv + c);
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), f2_pack(prm.scale_log2, prm.scale_log2),
-                         f2_pack(-l2.x, -l2.y)),
-                  x0, x1);
-        float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-        if (!full) {
-          p0 = (c >= lo && c < hi) ? p0 : 0.f;
-          p1 = (c + 1 >= lo && c + 1 < hi) ? p1 : 0.f;
-        }
-        pv[c] = p0;
-        pv[c + 1] = p1;
-        pk[c / 2] = pack_bf16x2(p0, p1);
+      for (int c = 0; c < BM; c += 4) {
+        const float4 l4 = lv[c / 4];
+        float x0, x1, x2, x3;
+        f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), sc2, f2_pack(l4.x, l4.y)), x0, x1);
+        f2_unpack(f2_fma(f2_pack(pv[c + 2], pv[c + 3]), sc2, f2_pack(l4.z, l4.w)), x2, x3);
+        pv[c] = fast_exp2(x0);
+        pv[c + 1] = fast_exp2(x1);
+        pv[c + 2] = fast_exp2(x2);
+        pv[c + 3] = fast_exp2(x3);
+        pk[c / 2] = pack_bf16x2(pv[c], pv[c + 1]);
+        pk[c / 2 + 1] = pack_bf16x2(pv[c + 2], pv[c + 3]);
       }
       tmem_st32(tm_s, pk);
       tmem_st32(tm_s + 32u, pk + 32);
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float* dv_ = dsum_s + vb * BM;
+      const float4* dv_ = reinterpret_cast<const float4*>(ndsum_s + vb * BM);
 #pragma unroll
       for (int c0 = 0; c0 < BM; c0 += 64) {
         float dp[64];
@@ -293,11 +294,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_wait_ld();
         uint32_t dk2[32];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float2 d2 = *reinterpret_cast<const float2*>(dv_ + c0 + c);
-          float a0, a1;
-          f2_unpack(f2_add(f2_pack(dp[c], dp[c + 1]), f2_pack(-d2.x, -d2.y)), a0, a1);
-          dk2[c / 2] = pack_bf16x2(pv[c0 + c] * a0, pv[c0 + c + 1] * a1);
+        for (int c = 0; c < 64; c += 4) {
+          const float4 d4 = dv_[(c0 + c) / 4];
+          float a0, a1, a2, a3;
+          f2_unpack(f2_mul(f2_add(f2_pack(dp[c], dp[c + 1]), f2_pack(d4.x, d4.y)), f2_pack(pv[c0 + c], pv[c0 + c + 1])),
+                    a0, a1);
+          f2_unpack(f2_mul(f2_add(f2_pack(dp[c + 2], dp[c + 3]), f2_pack(d4.z, d4.w)),
+                           f2_pack(pv[c0 + c + 2], pv[c0 + c + 3])),
+                    a2, a3);
+          dk2[c / 2] = pack_bf16x2(a0, a1);
+          dk2[c / 2 + 1] = pack_bf16x2(a2, a3);
         }
         // dS^T columns c0 .. c0 + 63 -> packed TMEM columns c0/2 .. c0/2 + 31 of the dP^T region
         // (those dP^T columns were read above, and later chunks read columns >= c0 + 64)
@@ -582,6 +588,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int64_t kvalid = L - (int64_t)kbk * BM;
       int hi = (int)min((int64_t)BM, kvalid);                                    // keys past the partition end
       if (prm.causal && kp == p && kbk == qb) hi = min(hi, row + 1);             // diagonal block
+      const bool any_mask = __any_sync(0xffffffffu, hi < BM);
       const uint32_t tm_s = tmem + lane_base + (uint32_t)((j & 1) * 128);
       ok = mbar_wait(bar(Ly::B_S + (j & 1)), (uint32_t)((j >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
                      ROLE_EW, j);
@@ -592,19 +599,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
       for (int c = 0; c < BM; c += 32) tmem_ld32(tm_s + (uint32_t)c, pv + c);
       tc_wait_ld();
+      // the S buffer is free once read: tell the MMA issuer (it may compute S(j+2) into it)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Ly::B_P));
+      if (any_mask) {
+#pragma unroll
+        for (int c = 0; c < BM; ++c)
+          if (c >= hi) pv[c] = -INFINITY;
+      }
       const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2);
       const uint64_t nl2 = f2_pack(-lse2, -lse2);
 #pragma unroll
       for (int c = 0; c < BM; c += 2) {
         float x0, x1;
         f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), sc2, nl2), x0, x1);
-        pv[c] = (c < hi) ? fast_exp2(x0) : 0.f;
-        pv[c + 1] = (c + 1 < hi) ? fast_exp2(x1) : 0.f;
+        pv[c] = fast_exp2(x0);
+        pv[c + 1] = fast_exp2(x1);
       }
-      // the S buffer is free once read: tell the MMA issuer (it may compute S(j+2) into it)
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(Ly::B_P));
       ok = mbar_wait(bar(Ly::B_DP), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, j);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -620,8 +632,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
           float a0, a1;
-          f2_unpack(f2_add(f2_pack(dp[c], dp[c + 1]), nd2), a0, a1);
-          ds2[c / 2] = pack_bf16x2(pv[c0 + c] * a0, pv[c0 + c + 1] * a1);
+          f2_unpack(f2_mul(f2_add(f2_pack(dp[c], dp[c + 1]), nd2), f2_pack(pv[c0 + c], pv[c0 + c + 1])), a0, a1);
+          ds2[c / 2] = pack_bf16x2(a0, a1);
         }
         tmem_st32(tm_dp + (uint32_t)(c0 / 2), ds2);
       }
