@@ -6,11 +6,12 @@
 // §"Mesh-Attention：从一维'环'到二维'网'"), with the forward's global LSE and D_i = dO_i . O_i:
 //   P_ij = exp(s_ij - LSE_i),  dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - D_i),
 //   dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j.
-// Two kernels; one CTA owns one 128-row tile of one unit (no persistence) with 6 warps:
-//   warps 0-3  elementwise: one thread per TMEM lane (a key row in dkdv, a query row in dq)
-//   warp 4     MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M = N = 128, K = 16, issued by an
+// Two kernels; one CTA owns one 128-row tile of one unit (no persistence) with 10 warps:
+//   warps 0-7  elementwise: two warps per TMEM lane quadrant, one thread per TMEM lane (a key row
+//              in dkdv, a query row in dq), each warp taking 64 of the block's 128 columns
+//   warp 8     MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M = N = 128, K = 16, issued by an
 //              elected lane of the converged warp; completion by tcgen05.commit
-//   warp 5     producer: TMA loads of 128 x 64 bf16 boxes with 128-byte swizzle
+//   warp 9     producer: TMA loads of 128 x 64 bf16 boxes with 128-byte swizzle
 //
 // dkdv (unit = KV slot, batch, KV head, 128-key block): K and V stay in shared memory; Q and dO
 // blocks of the slot's query rows (over the KV head's query heads) stream through three and two
@@ -41,9 +42,15 @@ namespace mesh {
 namespace btc {
 
 constexpr int BM = 128;  // rows per tile = TMEM lanes = keys / queries per block
-constexpr int NUM_THREADS = 192;
-constexpr int WARP_MMA = 4;
-constexpr int WARP_LOAD = 5;
+constexpr int NUM_THREADS = 320;
+constexpr int N_EW = 8;  // elementwise warps: two per TMEM lane quadrant, 64 columns each
+constexpr int WARP_MMA = 8;
+constexpr int WARP_LOAD = 9;
+// The bf16 P / dS written back into TMEM by column half `hf` land in packed columns
+// [64 hf, 64 hf + 32) of their region -- inside the half's own input columns, so the halves never
+// overwrite values the other still has to read -- and the MMAs that take them as A read K-step kk
+// (16 elements = 8 packed columns) from here:
+__device__ __forceinline__ uint32_t packed_col(int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); }
 constexpr int64_t DRAIN_NS = 200000000;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr int ROLE_EW = 1, ROLE_MMA = 2, ROLE_LOAD = 3, ROLE_ITEM = 4;
@@ -157,8 +164,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar(Ly::B_S), 1);
     mbar_init(bar(Ly::B_S + 1), 1);
     mbar_init(bar(Ly::B_DP), 1);
-    mbar_init(bar(Ly::B_P), 4);   // one lane of each elementwise warp
-    mbar_init(bar(Ly::B_DS), 4);
+    mbar_init(bar(Ly::B_P), N_EW);  // one lane of each elementwise warp
+    mbar_init(bar(Ly::B_DS), N_EW);
     mbar_init(bar(Ly::B_ACC), 1);
     mbar_init(bar(Ly::B_DRAIN), 1);
     mbar_init(bar(Ly::B_VEC), BM);  // every elementwise thread has written its LSE / D value
@@ -202,17 +209,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     qb = 0;
   };
 
-  if (warp < 4) {
+  if (warp < N_EW) {
     // ================================================================ elementwise
-    const int row = warp * 32 + lane;  // TMEM lane = key row within the block
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t tm_s = tmem + lane_base;             // S^T, then P^T (bf16) in its first half
-    const uint32_t tm_dp = tmem + lane_base + 128u;     // dP^T, then dS^T (bf16)
+    const int wq = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
+    const int row = wq * 32 + lane;           // TMEM lane = key row within the block
+    const int c_base = hf * 64;               // this warp's query columns [c_base, c_base + 64)
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t tm_s = tmem + lane_base;           // S^T, then P^T (bf16)
+    const uint32_t tm_dp = tmem + lane_base + 128u;   // dP^T, then dS^T (bf16)
     const uint32_t tm_dv = tmem + lane_base + 256u;
     const uint32_t tm_dk = tmem + lane_base + 256u + (uint32_t)D;
     const int64_t key_local = (int64_t)kb * BM + row;
     bool ok = run;
-    // LSE / D of the next block's query columns, loaded one block ahead by thread `row`
+    // -LSE log2 e / -D of query column `row`, loaded one block ahead by the first column half
     float nxt_lse = 0.f, nxt_d = 0.f;
     auto fetch = [&](int i) {
       int h, p, qb;
@@ -227,15 +236,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         nxt_d = 0.f;
       }
     };
-    if (ok && NBQ > 0) fetch(0);
+    if (ok && NBQ > 0 && hf == 0) fetch(0);
     for (int i = 0; i < NBQ && ok; ++i) {
       const int vb = i & 1;
-      // publish this row's LSE / D, then wait (bounded) until all 128 columns are written; a
-      // buffer is rewritten two blocks later, after every thread has arrived for the block between
-      nlse_s[vb * BM + row] = nxt_lse;
-      ndsum_s[vb * BM + row] = nxt_d;
-      mbar_arrive(bar(Ly::B_VEC + vb));
-      if (i + 1 < NBQ) fetch(i + 1);
+      // publish this column's values, then wait (bounded) until all 128 columns are written; a
+      // buffer is rewritten two blocks later, after every writer has arrived for the block between
+      if (hf == 0) {
+        nlse_s[vb * BM + row] = nxt_lse;
+        ndsum_s[vb * BM + row] = nxt_d;
+        mbar_arrive(bar(Ly::B_VEC + vb));
+        if (i + 1 < NBQ) fetch(i + 1);
+      }
       ok = mbar_wait(bar(Ly::B_VEC + vb), (uint32_t)((i >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
                      ROLE_EW, i);
       ok = __all_sync(0xffffffffu, ok);
@@ -245,25 +256,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       (void)h;
       // causal diagonal block: query columns before this key row are masked (query rows past the
       // partition end carry -inf in place of -LSE and need no mask)
-      const int lo = (prm.causal && p == k && qb == kb) ? row : 0;
+      const int lo = (prm.causal && p == k && qb == kb) ? row - c_base : 0;
       ok = mbar_wait(bar(Ly::B_S), (uint32_t)(i & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, i);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      float pv[BM];
-#pragma unroll
-      for (int c = 0; c < BM; c += 32) tmem_ld32(tm_s + (uint32_t)c, pv + c);
+      float pv[64];
+      tmem_ld32(tm_s + (uint32_t)c_base, pv);
+      tmem_ld32(tm_s + (uint32_t)c_base + 32u, pv + 32);
       tc_wait_ld();
       if (__any_sync(0xffffffffu, lo > 0)) {
 #pragma unroll
-        for (int c = 0; c < BM; ++c)
+        for (int c = 0; c < 64; ++c)
           if (c < lo) pv[c] = -INFINITY;
       }
-      const float4* lv = reinterpret_cast<const float4*>(nlse_s + vb * BM);
+      const float4* lv = reinterpret_cast<const float4*>(nlse_s + vb * BM + c_base);
       const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2);
-      uint32_t pk[BM / 2];
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < BM; c += 4) {
+      for (int c = 0; c < 64; c += 4) {
         const float4 l4 = lv[c / 4];
         float x0, x1, x2, x3;
         f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), sc2, f2_pack(l4.x, l4.y)), x0, x1);
@@ -275,8 +286,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         pk[c / 2] = pack_bf16x2(pv[c], pv[c + 1]);
         pk[c / 2 + 1] = pack_bf16x2(pv[c + 2], pv[c + 3]);
       }
-      tmem_st32(tm_s, pk);
-      tmem_st32(tm_s + 32u, pk + 32);
+      tmem_st32(tm_s + (uint32_t)c_base, pk);  // P^T columns of this half (see packed_col)
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -285,36 +295,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const float4* dv_ = reinterpret_cast<const float4*>(ndsum_s + vb * BM);
-#pragma unroll
-      for (int c0 = 0; c0 < BM; c0 += 64) {
+      {
         float dp[64];
-        tmem_ld32(tm_dp + (uint32_t)c0, dp);
-        tmem_ld32(tm_dp + (uint32_t)c0 + 32u, dp + 32);
+        tmem_ld32(tm_dp + (uint32_t)c_base, dp);
+        tmem_ld32(tm_dp + (uint32_t)c_base + 32u, dp + 32);
         tc_wait_ld();
-        uint32_t dk2[32];
+        const float4* dv_ = reinterpret_cast<const float4*>(ndsum_s + vb * BM + c_base);
+        uint32_t ds2[32];
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
-          const float4 d4 = dv_[(c0 + c) / 4];
+          const float4 d4 = dv_[c / 4];
           float a0, a1, a2, a3;
-          f2_unpack(f2_mul(f2_add(f2_pack(dp[c], dp[c + 1]), f2_pack(d4.x, d4.y)), f2_pack(pv[c0 + c], pv[c0 + c + 1])),
-                    a0, a1);
-          f2_unpack(f2_mul(f2_add(f2_pack(dp[c + 2], dp[c + 3]), f2_pack(d4.z, d4.w)),
-                           f2_pack(pv[c0 + c + 2], pv[c0 + c + 3])),
+          f2_unpack(f2_mul(f2_add(f2_pack(dp[c], dp[c + 1]), f2_pack(d4.x, d4.y)), f2_pack(pv[c], pv[c + 1])), a0, a1);
+          f2_unpack(f2_mul(f2_add(f2_pack(dp[c + 2], dp[c + 3]), f2_pack(d4.z, d4.w)), f2_pack(pv[c + 2], pv[c + 3])),
                     a2, a3);
-          dk2[c / 2] = pack_bf16x2(a0, a1);
-          dk2[c / 2 + 1] = pack_bf16x2(a2, a3);
+          ds2[c / 2] = pack_bf16x2(a0, a1);
+          ds2[c / 2 + 1] = pack_bf16x2(a2, a3);
         }
-        // dS^T columns c0 .. c0 + 63 -> packed TMEM columns c0/2 .. c0/2 + 31 of the dP^T region
-        // (those dP^T columns were read above, and later chunks read columns >= c0 + 64)
-        tmem_st32(tm_dp + (uint32_t)(c0 / 2), dk2);
+        tmem_st32(tm_dp + (uint32_t)c_base, ds2);  // dS^T columns of this half
       }
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(Ly::B_DS));
     }
-    // ---- epilogue: dV and dK rows of this key block
+    // ---- epilogue: this half's columns of the dV and dK rows of this key block
     if (ok) {
       ok = mbar_wait(bar(Ly::B_ACC), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, -1);
       ok = __all_sync(0xffffffffu, ok);
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const int64_t prow = (((int64_t)b * prm.Hkv + hk) * prm.n_kv_slots + it.slot) * L + key_local;
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
+      for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
         float v[32], kk[32];
         tmem_ld32(tm_dv + (uint32_t)c, v);
         tmem_ld32(tm_dk + (uint32_t)c, kk);
@@ -369,14 +374,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t gd = b_mn + (uint64_t)sbb * TILE16;
 #pragma unroll
       for (int kk = 0; kk < BM / 16; ++kk)
-        tc_mma_ts_warp(tmem + 256u, tmem + (uint32_t)(kk * 8), gd + (uint64_t)(kk * 128), idesc_ts,
+        tc_mma_ts_warp(tmem + 256u, tmem + packed_col(kk), gd + (uint64_t)(kk * 128), idesc_ts,
                        (!first || kk > 0) ? 1u : 0u);
     };
     auto issue_dk = [&](int sa, bool first) {  // dK += dS^T Q
       const uint64_t qd = a_mn + (uint64_t)sa * TILE16;
 #pragma unroll
       for (int kk = 0; kk < BM / 16; ++kk)
-        tc_mma_ts_warp(tmem + 256u + (uint32_t)D, tmem + 128u + (uint32_t)(kk * 8), qd + (uint64_t)(kk * 128),
+        tc_mma_ts_warp(tmem + 256u + (uint32_t)D, tmem + 128u + packed_col(kk), qd + (uint64_t)(kk * 128),
                        idesc_ts, (!first || kk > 0) ? 1u : 0u);
     };
     auto wait_a = [&](int i) {  // Q(i) landed
@@ -529,8 +534,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar(Ly::B_S), 1);
     mbar_init(bar(Ly::B_S + 1), 1);
     mbar_init(bar(Ly::B_DP), 1);
-    mbar_init(bar(Ly::B_P), 4);
-    mbar_init(bar(Ly::B_DS), 4);
+    mbar_init(bar(Ly::B_P), N_EW);
+    mbar_init(bar(Ly::B_DS), N_EW);
     mbar_init(bar(Ly::B_ACC), 1);
     mbar_init(bar(Ly::B_DRAIN), 1);
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0 || !unit_ok) ? 1 : 0;
@@ -570,10 +575,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     kbk = 0;
   };
 
-  if (warp < 4) {
+  if (warp < N_EW) {
     // ================================================================ elementwise
-    const int row = warp * 32 + lane;  // TMEM lane = query row within the block
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int wq = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
+    const int row = wq * 32 + lane;           // TMEM lane = query row within the block
+    const int c_base = hf * 64;               // this warp's key columns [c_base, c_base + 64)
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const uint32_t tm_dp = tmem + lane_base + 256u;  // dP, then dS (bf16)
     const uint32_t tm_dq = tmem + lane_base + 384u;
     const int64_t q_local = (int64_t)qb * BM + row;
@@ -586,18 +593,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int kp, kbk;
       block_at(j, kp, kbk);
       const int64_t kvalid = L - (int64_t)kbk * BM;
-      int hi = (int)min((int64_t)BM, kvalid);                                    // keys past the partition end
-      if (prm.causal && kp == p && kbk == qb) hi = min(hi, row + 1);             // diagonal block
-      const bool any_mask = __any_sync(0xffffffffu, hi < BM);
+      int hi = (int)min((int64_t)BM, kvalid);                         // keys past the partition end
+      if (prm.causal && kp == p && kbk == qb) hi = min(hi, row + 1);  // diagonal block
+      hi -= c_base;                                                   // in this half's columns
+      const bool any_mask = __any_sync(0xffffffffu, hi < 64);
       const uint32_t tm_s = tmem + lane_base + (uint32_t)((j & 1) * 128);
       ok = mbar_wait(bar(Ly::B_S + (j & 1)), (uint32_t)((j >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
                      ROLE_EW, j);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      float pv[BM];
-#pragma unroll
-      for (int c = 0; c < BM; c += 32) tmem_ld32(tm_s + (uint32_t)c, pv + c);
+      float pv[64];
+      tmem_ld32(tm_s + (uint32_t)c_base, pv);
+      tmem_ld32(tm_s + (uint32_t)c_base + 32u, pv + 32);
       tc_wait_ld();
       // the S buffer is free once read: tell the MMA issuer (it may compute S(j+2) into it)
       tc_fence_before();
@@ -605,13 +613,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(bar(Ly::B_P));
       if (any_mask) {
 #pragma unroll
-        for (int c = 0; c < BM; ++c)
+        for (int c = 0; c < 64; ++c)
           if (c >= hi) pv[c] = -INFINITY;
       }
       const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2);
       const uint64_t nl2 = f2_pack(-lse2, -lse2);
 #pragma unroll
-      for (int c = 0; c < BM; c += 2) {
+      for (int c = 0; c < 64; c += 2) {
         float x0, x1;
         f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), sc2, nl2), x0, x1);
         pv[c] = fast_exp2(x0);
@@ -621,21 +629,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint64_t nd2 = f2_pack(-dsum, -dsum);
-#pragma unroll
-      for (int c0 = 0; c0 < BM; c0 += 64) {
+      {
+        const uint64_t nd2 = f2_pack(-dsum, -dsum);
         float dp[64];
-        tmem_ld32(tm_dp + (uint32_t)c0, dp);
-        tmem_ld32(tm_dp + (uint32_t)c0 + 32u, dp + 32);
+        tmem_ld32(tm_dp + (uint32_t)c_base, dp);
+        tmem_ld32(tm_dp + (uint32_t)c_base + 32u, dp + 32);
         tc_wait_ld();
         uint32_t ds2[32];
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
           float a0, a1;
-          f2_unpack(f2_mul(f2_add(f2_pack(dp[c], dp[c + 1]), nd2), f2_pack(pv[c0 + c], pv[c0 + c + 1])), a0, a1);
+          f2_unpack(f2_mul(f2_add(f2_pack(dp[c], dp[c + 1]), nd2), f2_pack(pv[c], pv[c + 1])), a0, a1);
           ds2[c / 2] = pack_bf16x2(a0, a1);
         }
-        tmem_st32(tm_dp + (uint32_t)(c0 / 2), ds2);
+        tmem_st32(tm_dp + (uint32_t)c_base, ds2);  // dS columns of this half (see packed_col)
       }
       tc_wait_st();
       tc_fence_before();
@@ -650,7 +657,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const int64_t prow = (((int64_t)b * prm.Hq + h) * prm.n_slots + it.slot) * L + q_local;
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
+      for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
         float v[32];
         tmem_ld32(tm_dq + (uint32_t)c, v);
         tc_wait_ld();
@@ -692,7 +699,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t kd = a_mn + (uint64_t)sa * TILE16;
 #pragma unroll
       for (int kk = 0; kk < BM / 16; ++kk)
-        tc_mma_ts_warp(tmem + 384u, tmem + 256u + (uint32_t)(kk * 8), kd + (uint64_t)(kk * 128), idesc_ts,
+        tc_mma_ts_warp(tmem + 384u, tmem + 256u + packed_col(kk), kd + (uint64_t)(kk * 128), idesc_ts,
                        (!first || kk > 0) ? 1u : 0u);
     };
     auto wait_a = [&](int j) {  // K(j) landed
