@@ -377,7 +377,7 @@ def main():
     else:
         plan = m.mesh_attn_plan_create(w.S, w.P, w.causal, w.kvr, w.greedy)
     po, pl = m.new_partials(plan, w.B, w.Hq, w.d, dev)
-    wsp = m.new_workspace(plan, dev)
+    wsp = m.new_workspace(plan, dev, qd, kd)
     st = m.new_status(dev)
     O = torch.empty_like(qd)
     LSE = torch.empty(w.B, w.Hq, w.S, dtype=torch.float32, device=dev)

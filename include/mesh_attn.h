@@ -147,17 +147,28 @@ int mesh_attn_plan_volumes(const mesh_attn_plan* plan, int32_t Hq, int32_t Hkv, 
 int mesh_attn_partials_size(const mesh_attn_plan* plan, int32_t B, int32_t Hq, int32_t d,
                             size_t* o_elems, size_t* lse_elems);
 
-/* Bytes of device workspace mesh_attn_tile_fwd and mesh_attn_merge need for this plan (the
- * plan's work list, slot offsets and a scheduling counter).  The caller allocates it (16-byte
- * aligned) and may reuse it across calls on one stream; calls that overlap on the GPU need
- * separate workspaces. */
+/* Bytes of device workspace mesh_attn_tile_fwd with bf16 inputs, and mesh_attn_merge, need for
+ * this plan (the plan's work list, slot offsets and a scheduling counter).  The caller allocates
+ * it (16-byte aligned) and may reuse it across calls on one stream; calls that overlap on the GPU
+ * need separate workspaces. */
 int mesh_attn_workspace_size(const mesh_attn_plan* plan, size_t* bytes);
+
+/* Bytes of device workspace mesh_attn_tile_fwd needs for inputs of `in_dtype` and these sizes:
+ * the above for MESH_ATTN_BF16; for MESH_ATTN_F32 also room for the bf16 pieces the fp32 path
+ * splits Q, K and V into, 6 * (B*Hq + 2*B*Hkv) * S * d bytes (see mesh_attn_tile_fwd).  Enough for
+ * mesh_attn_merge as well. */
+int mesh_attn_workspace_size_for(const mesh_attn_plan* plan, mesh_attn_dtype in_dtype, int32_t B,
+                                 int32_t Hq, int32_t Hkv, int32_t d, size_t* bytes);
 
 /* Tile attention forward: every (Q partition, tile) item of the plan, for every batch and
  * query head, writes its partial O_t and lse_t (step 2 above).
  *   in_dtype  MESH_ATTN_BF16 (tensor-core kernel: bf16 products, fp32 accumulation, fp32
- *             online softmax, P rounded to bf16 for the PV product) or MESH_ATTN_F32 (fp32
- *             CUDA-core kernel, fp32 throughout).
+ *             online softmax, P rounded to bf16 for the PV product) or MESH_ATTN_F32 (tensor-core
+ *             kernel with fp32 accuracy: Q, K, V and P are each split exactly into three bf16
+ *             pieces x = x1 + x2 + x3 and every product sums the six piece products of order
+ *             >= 2^-16, x1y1 + x1y2 + x2y1 + x1y3 + x3y1 + x2y2, with fp32 accumulation; the
+ *             pieces go into the workspace, which must then hold mesh_attn_workspace_size_for
+ *             bytes).
  *   d         64 or 128.  B >= 0, Hq >= 0, Hkv >= 1, Hq % Hkv == 0.
  *   Q, K, V   device tensors of in_dtype, 16-byte aligned (layouts above).
  *   scale     softmax scale, finite and > 0 (1/sqrt(d) is the usual choice).
@@ -183,9 +194,10 @@ int mesh_attn_tile_fwd(const mesh_attn_plan* plan, mesh_attn_dtype in_dtype, int
  * pre-reserved memory budget -- and so cannot provide the workspace mesh_attn_tile_fwd asks
  * for.  It computes exactly what mesh_attn_tile_fwd computes, with the same arguments minus
  * the workspace; the caller still passes the inputs, the partial outputs and d_status.
- * The plan's work list goes into one fixed array of MESH_ATTN_NOALLOC_SCRATCH_BYTES inside the
- * library instead.  A plan whose work list needs more (about 2.6 MB for P = 1024 causal; P =
- * 4096 is too large) returns MESH_ATTN_ERR_WORKSPACE with the size in mesh_attn_last_error().
+ * The plan's work list (and, for fp32 inputs, the bf16 pieces of Q, K and V) goes into one fixed
+ * array of MESH_ATTN_NOALLOC_SCRATCH_BYTES inside the library instead.  A call that needs more
+ * (a work list of about 2.6 MB for P = 1024 causal; P = 4096 is too large; fp32 inputs above
+ * about 4 MB of pieces) returns MESH_ATTN_ERR_WORKSPACE with the size in mesh_attn_last_error().
  * The first call on a device looks up that device's array address (cudaGetSymbolAddress with
  * the device current); make that first call before any stream capture.  No cudaMalloc, cudaFree
  * or other allocating call is made.  All calls on a device share the one array and each call

@@ -257,3 +257,19 @@ def test_backward_sizes_and_status_codes(lib):
                                  None, None, 0, None, None) == 0
     assert so.mesh_attn_bwd_reduce(empty.handle, 1, 1, 2, 1, 128, None, None, None, None, None, None, None, 0, None,
                                    None) == 0
+
+
+def test_workspace_size_for_fp32_pieces(lib):
+    """fp32 inputs need room for three bf16 pieces of Q, K and V after the work list; bf16 inputs
+    need the work list only."""
+    p = lib.mesh_attn_plan_create(16384, 16, True)
+    base = lib.mesh_attn_workspace_size(p)
+    assert lib.mesh_attn_workspace_size_for(p, lib.torch.bfloat16, 1, 16, 4, 128) == base
+    up = lambda x: (x + 255) // 256 * 256
+    q, kv = 3 * 16 * 16384 * 128 * 2, 3 * 4 * 16384 * 128 * 2
+    assert lib.mesh_attn_workspace_size_for(p, lib.torch.float32, 1, 16, 4, 128) == up(base) + up(q) + 2 * up(kv)
+    fake = ctypes.c_void_p(1 << 20)
+    so = lib._lib
+    # an fp32 call with only the bf16-sized workspace is refused before anything is enqueued
+    assert so.mesh_attn_tile_fwd(p.handle, 0, 1, 16, 4, 128, fake, fake, fake, 0.1, fake, fake, fake, base, fake,
+                                 None) == 9

@@ -23,6 +23,7 @@ pytestmark = pytest.mark.gpu
 CASES = [
     Workload(130, "noalloc_gqa_causal", 1, 4, 2, 4096, 128, "bf16", True, 16),
     Workload(131, "noalloc_ragged", 1, 2, 1, 800, 128, "bf16", False, 4),
+    Workload(132, "noalloc_f32_pieces_in_scratch", 1, 2, 2, 512, 64, "f32", True, 4),
 ]
 
 
@@ -31,7 +32,7 @@ def test_noalloc_matches_workspace_entry_point(lib):
         q, k, v = (t.cuda() for t in make_qkv(w))
         plan = lib.mesh_attn_plan_create(w.S, w.P, w.causal, w.kvr, w.greedy)
         ref_o, ref_l = lib.new_partials(plan, w.B, w.Hq, w.d)
-        ws = lib.new_workspace(plan)
+        ws = lib.new_workspace(plan, "cuda", q, k)
         st_ref = lib.new_status()
         lib.mesh_attn_tile_fwd(plan, q, k, v, None, ref_o, ref_l, ws, st_ref)
         out_o, out_l = lib.new_partials(plan, w.B, w.Hq, w.d)

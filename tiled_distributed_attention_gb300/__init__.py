@@ -54,6 +54,7 @@ _SIGS = {
     "mesh_attn_plan_volumes": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, P_i32, P_i64, P_i64]),
     "mesh_attn_partials_size": (c_i32, [c_vp, c_i32, c_i32, c_i32, P_sz, P_sz]),
     "mesh_attn_workspace_size": (c_i32, [c_vp, P_sz]),
+    "mesh_attn_workspace_size_for": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, P_sz]),
     "mesh_attn_tile_fwd": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_f32, c_vp, c_vp,
                                    c_vp, c_sz, c_vp, c_vp]),
     "mesh_attn_tile_fwd_noalloc": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_f32, c_vp,
@@ -217,13 +218,28 @@ def mesh_attn_workspace_size(plan: Plan) -> int:
     return n.value
 
 
+def mesh_attn_workspace_size_for(plan: Plan, dtype: torch.dtype, B: int, Hq: int, Hkv: int, d: int) -> int:
+    n = c_sz()
+    _check(_lib.mesh_attn_workspace_size_for(plan.handle, _dtype_code(dtype), B, Hq, Hkv, d, ctypes.byref(n)),
+           "mesh_attn_workspace_size_for")
+    return n.value
+
+
 def new_status(device=None) -> torch.Tensor:
     """A zeroed device status block (MESH_ATTN_STATUS_WORDS int32)."""
     return torch.zeros(MESH_ATTN_STATUS_WORDS, dtype=torch.int32, device=device or "cuda")
 
 
-def new_workspace(plan: Plan, device=None) -> torch.Tensor:
-    return torch.empty(max(mesh_attn_workspace_size(plan), 16), dtype=torch.uint8, device=device or "cuda")
+def new_workspace(plan: Plan, device=None, q: Optional[torch.Tensor] = None, k: Optional[torch.Tensor] = None
+                  ) -> torch.Tensor:
+    """Workspace for mesh_attn_tile_fwd and mesh_attn_merge; pass q and k (fp32 inputs need room
+    for their bf16 pieces)."""
+    if q is not None and k is not None:
+        B, Hq, _, d = q.shape
+        n = mesh_attn_workspace_size_for(plan, q.dtype, B, Hq, k.shape[1], d)
+    else:
+        n = mesh_attn_workspace_size(plan)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
 
 
 def new_partials(plan: Plan, B: int, Hq: int, d: int, device=None):
@@ -398,7 +414,7 @@ def mesh_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, ca
     B, Hq, S, d = q.shape
     plan = plan or mesh_attn_plan_create(S, P, causal, kvr, greedy)
     po, pl = new_partials(plan, B, Hq, d, q.device)
-    ws = new_workspace(plan, q.device)
+    ws = new_workspace(plan, q.device, q, k)
     st = new_status(q.device)
     O = torch.empty_like(q)
     LSE = torch.empty(B, Hq, S, dtype=torch.float32, device=q.device)

@@ -209,6 +209,21 @@ int mesh_attn_workspace_size(const mesh_attn_plan* plan, size_t* bytes) {
   });
 }
 
+int mesh_attn_workspace_size_for(const mesh_attn_plan* plan, mesh_attn_dtype in_dtype, int32_t B, int32_t Hq,
+                                 int32_t Hkv, int32_t d, size_t* bytes) {
+  return guarded([&] {
+    if (!plan || !bytes) return fail(MESH_ATTN_ERR_INVALID_ARG, "NULL argument");
+    if (in_dtype != MESH_ATTN_F32 && in_dtype != MESH_ATTN_BF16)
+      return fail(MESH_ATTN_ERR_INVALID_ARG, "in_dtype must be MESH_ATTN_F32 or MESH_ATTN_BF16");
+    if (B < 0 || Hq < 0 || Hkv < 0 || d < 0) return fail(MESH_ATTN_ERR_INVALID_ARG, "B, Hq, Hkv and d must be >= 0");
+    const size_t base = mesh::workspace_layout(plan->p).total;
+    *bytes = in_dtype == MESH_ATTN_F32
+                 ? ((base + 255) & ~(size_t)255) + mesh::f32_pieces_layout(B, Hq, Hkv, plan->p.S, d).total
+                 : base;
+    return (int)MESH_ATTN_OK;
+  });
+}
+
 int mesh_attn_tile_fwd(const mesh_attn_plan* plan, mesh_attn_dtype in_dtype, int32_t B, int32_t Hq, int32_t Hkv,
                        int32_t d, const void* Q, const void* K, const void* V, float scale, float* partial_o,
                        float* partial_lse, void* workspace, size_t workspace_bytes, int32_t* d_status,
@@ -228,8 +243,12 @@ int mesh_attn_tile_fwd(const mesh_attn_plan* plan, mesh_attn_dtype in_dtype, int
         !aligned(partial_lse, 4) || !aligned(workspace, 16) || !aligned(d_status, 4))
       return fail(MESH_ATTN_ERR_MISALIGNED, "Q, K, V, partial_o and workspace must be 16-byte aligned");
     const mesh::WorkspaceLayout wl = mesh::workspace_layout(pl);
-    if (workspace_bytes < wl.total)
-      return fail(MESH_ATTN_ERR_WORKSPACE, "workspace needs " + std::to_string(wl.total) + " bytes");
+    // fp32 inputs: the bf16 pieces of Q, K and V follow the work list
+    const size_t pieces_off = (wl.total + 255) & ~(size_t)255;
+    const size_t need = in_dtype == MESH_ATTN_F32 ? pieces_off + mesh::f32_pieces_layout(B, Hq, Hkv, pl.S, d).total
+                                                  : wl.total;
+    if (workspace_bytes < need)
+      return fail(MESH_ATTN_ERR_WORKSPACE, "workspace needs " + std::to_string(need) + " bytes");
     char* ws = static_cast<char*>(workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemcpyAsync(ws + wl.items_off, pl.dev_items.data(), wl.items_bytes, cudaMemcpyHostToDevice, st);
@@ -261,9 +280,10 @@ int mesh_attn_tile_fwd(const mesh_attn_plan* plan, mesh_attn_dtype in_dtype, int
     a.scale = scale;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
     a.wait_limit_ns = g_wait_limit_ns.load();
+    a.pieces = ws + pieces_off;
     std::string err;
     const int ce = (in_dtype == MESH_ATTN_BF16) ? mesh::launch_tile_fwd_tc(a, stream, &err)
-                                                : mesh::launch_tile_fwd_simt(a, MESH_ATTN_F32, stream, &err);
+                                                : mesh::launch_tile_fwd_tc32(a, stream, &err);
     if (ce != (int)cudaSuccess) return fail(MESH_ATTN_ERR_CUDA, err.empty() ? cudaGetErrorString((cudaError_t)ce) : err);
     return (int)MESH_ATTN_OK;
   });

@@ -75,10 +75,17 @@ struct TileArgs {
   float scale;
   float scale_log2;
   int64_t wait_limit_ns;
+  void* pieces;  // fp32 inputs: device buffer for the bf16 pieces of Q, K and V (f32_pieces_layout)
 };
 // Kernel launchers return a cudaError_t value as int; *err gets a message on failure.
-int launch_tile_fwd_simt(const TileArgs& a, mesh_attn_dtype dt, void* stream, std::string* err);
 int launch_tile_fwd_tc(const TileArgs& a, void* stream, std::string* err);
+// fp32 inputs: split Q, K and V into bf16 pieces in a.pieces, then the tensor-core forward.
+int launch_tile_fwd_tc32(const TileArgs& a, void* stream, std::string* err);
+// Byte layout of the bf16 pieces of fp32 Q, K and V ([3][rows][d] each, 256-byte aligned parts).
+struct F32Pieces {
+  size_t q_off, k_off, v_off, total;
+};
+F32Pieces f32_pieces_layout(int32_t B, int32_t Hq, int32_t Hkv, int64_t S, int32_t d);
 
 struct MergeArgs {
   const float* part_o;

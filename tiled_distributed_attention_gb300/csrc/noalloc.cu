@@ -72,11 +72,15 @@ extern "C" int mesh_attn_tile_fwd_noalloc(const mesh_attn_plan* plan, mesh_attn_
     const size_t items_off = 0;
     const size_t kv_off = (wl.items_bytes + 255) & ~(size_t)255;
     const size_t counter_off = kv_off + ((wl.kv_bytes + 255) & ~(size_t)255);
-    const size_t need = counter_off + 256;
+    // fp32 inputs also keep the bf16 pieces of Q, K and V in the scratch
+    const size_t pieces_off = counter_off + 256;
+    const size_t need = in_dtype == MESH_ATTN_F32 ? pieces_off + mesh::f32_pieces_layout(B, Hq, Hkv, pl.S, d).total
+                                                  : pieces_off;
     if (need > MESH_ATTN_NOALLOC_SCRATCH_BYTES)
       return noalloc_fail(MESH_ATTN_ERR_WORKSPACE,
-                          "plan work list needs " + std::to_string(need) + " bytes of scratch; the no-allocation "
-                          "entry point holds at most " + std::to_string((size_t)MESH_ATTN_NOALLOC_SCRATCH_BYTES) +
+                          "plan work list (and fp32 input pieces) need " + std::to_string(need) +
+                          " bytes of scratch; the no-allocation entry point holds at most " +
+                          std::to_string((size_t)MESH_ATTN_NOALLOC_SCRATCH_BYTES) +
                           " bytes: use mesh_attn_tile_fwd with a workspace");
     if (pl.n_slots() == 0 || B == 0 || Hq == 0) return noalloc_fail(MESH_ATTN_OK, "");
     if (!Q || !K || !V || !partial_o || !partial_lse || !d_status)
@@ -119,9 +123,10 @@ extern "C" int mesh_attn_tile_fwd_noalloc(const mesh_attn_plan* plan, mesh_attn_
     a.scale = scale;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
     a.wait_limit_ns = mesh::current_wait_limit_ns();
+    a.pieces = ws + pieces_off;
     std::string err;
     const int ce = (in_dtype == MESH_ATTN_BF16) ? mesh::launch_tile_fwd_tc(a, stream, &err)
-                                                : mesh::launch_tile_fwd_simt(a, MESH_ATTN_F32, stream, &err);
+                                                : mesh::launch_tile_fwd_tc32(a, stream, &err);
     if (ce != (int)cudaSuccess)
       return noalloc_fail(MESH_ATTN_ERR_CUDA, err.empty() ? cudaGetErrorString((cudaError_t)ce) : err);
     return noalloc_fail(MESH_ATTN_OK, "");

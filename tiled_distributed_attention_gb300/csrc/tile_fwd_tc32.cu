@@ -1,0 +1,497 @@
+// Tile attention forward for fp32 inputs on the 5th-generation tensor cores (sm_103a), with fp32
+// accuracy: every fp32 operand x is split exactly into three bf16 pieces x = x1 + x2 + x3
+// (8 + 8 + 8 significant bits: x1 = bf16(x), x2 = bf16(x - x1), x3 = bf16(x - x1 - x2)), and a
+// product sums the six piece products whose order is at least 2^-16 of the whole,
+//   x1 y1 + x1 y2 + x2 y1 + x1 y3 + x3 y1 + x2 y2,
+// on bf16 tensor-core products with fp32 accumulation; the terms left out are O(2^-24).  Six
+// bf16 products cost what three tf32 products cost.
+//
+// Same work decomposition and outputs as the bf16 kernel (Mesh-Attention tiles and partial
+// outputs: "Mesh-Attention: A New Communication-Efficient Distributed Attention with Improved
+// Data Locality", tutorial §"Mesh-Attention：从一维'环'到二维'网'"; online m_i / l_i softmax of
+// "环形注意力：突破长序列处理瓶颈的分布式计算范式", §"数值稳定性：Log-Sum-Exp技术的分布式应用").
+//   split_kernel: Q, K and V into their bf16 pieces, [3][rows][d] each, in the caller's
+//                 workspace (HBM-bound, one pass).
+//   tile_fwd_tc32_kernel: one CTA per (work item, batch, head, 128-row query tile); 6 warps --
+//     warps 0-3 softmax (one thread per row = TMEM lane), warp 4 MMA issuer (elected lane of a
+//     converged warp), warp 5 TMA producer.  64-key blocks keep the three pieces of Q, K and V of
+//     a d = 128 block within shared memory (96 + 48 + 48 KB).  TMEM: S (64 columns; P's first and
+//     second pieces are written back as bf16 into them) | P's third piece (32) | O (d).  The row
+//     maximum is exact every block (no deferred reference), P is split into its three pieces in
+//     registers.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <string>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mesh {
+namespace tc32 {
+
+constexpr int BM = 128;  // query rows per tile = TMEM lanes
+constexpr int BN = 64;   // keys per block
+constexpr int NUM_THREADS = 192;
+constexpr int WARP_MMA = 4;
+constexpr int WARP_LOAD = 5;
+constexpr int NPAIR = 6;
+constexpr int64_t DRAIN_NS = 200000000;
+constexpr int ROLE_SOFTMAX = 1, ROLE_MMA = 2, ROLE_LOAD = 3, ROLE_ITEM = 4;
+
+// piece pairs (a, b) of a product: x_a y_b
+__device__ __forceinline__ int pair_a(int i) { return i == 2 ? 1 : i == 4 ? 2 : i == 5 ? 1 : 0; }
+__device__ __forceinline__ int pair_b(int i) { return i == 1 ? 1 : i == 3 ? 2 : i == 5 ? 1 : 0; }
+
+struct Params {
+  const DevItem* items;
+  const int32_t* kv_list;
+  float* part_o;
+  float* part_lse;
+  int32_t* status;
+  int64_t S, L;
+  int64_t q_rows, kv_rows;  // rows of one piece: B*Hq*S and B*Hkv*S
+  int32_t B, Hq, Hkv, P, n_items, n_slots, nqt, nb, causal;
+  float scale_log2;
+  int64_t wait_limit_ns;
+};
+
+template <int D>
+struct Layout {
+  static constexpr uint32_t QP = BM * D * 2;    // one piece of the Q tile
+  static constexpr uint32_t KP = BN * D * 2;    // one piece of a K or V block
+  static constexpr uint32_t QBOX = BM * 128;    // 128 rows x 64 bf16 columns
+  static constexpr uint32_t KBOX = BN * 128;    // 64 rows x 64 bf16 columns
+  static constexpr uint32_t Q_OFF = 0, K_OFF = 3 * QP, V_OFF = K_OFF + 3 * KP;
+  static constexpr uint32_t BAR_OFF = V_OFF + 3 * KP;
+  static constexpr int B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 2, B_SFULL = 3, B_PFULL = 4, B_OFULL = 5, B_DRAIN = 6,
+                       NBARS = 7;
+  static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;
+  static constexpr uint32_t TOTAL = MISC_OFF + 16;
+};
+
+// 64-key blocks of KV partition k seen by query tile qt of partition p: on the causal diagonal
+// partition only the blocks up to the tile's last row.
+__device__ __forceinline__ int kblocks(int k, int p, int causal, int nb, int qt) {
+  return (causal && k == p) ? min(nb, 2 * qt + 2) : nb;
+}
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tile_fwd_tc32_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const Params prm) {
+  using Ly = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sb = smem_u32(smem_raw);
+  if (sb & 1023u) {  // 128-byte swizzle atoms need 1024-aligned operands; no room to align by hand
+    if (threadIdx.x == 0) record_error(prm.status, MESH_ATTN_ERR_INTERNAL, ROLE_ITEM, (int32_t)blockIdx.x);
+    return;
+  }
+  uint8_t* smem = smem_raw;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return sb + Ly::BAR_OFF + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::MISC_OFF);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + Ly::MISC_OFF + 4);
+  const int64_t L = prm.L;
+
+  int64_t uu = blockIdx.x;
+  const int qt = (int)(uu % prm.nqt); uu /= prm.nqt;
+  const int h = (int)(uu % prm.Hq); uu /= prm.Hq;
+  const int b = (int)(uu % prm.B);
+  const int idx = (int)(uu / prm.B);
+  const DevItem it = prm.items[idx];
+  const bool unit_ok = it.p >= 0 && it.p < prm.P && it.slot >= 0 && it.slot < prm.n_slots && it.n_kv >= 1 &&
+                       it.kv_off >= 0;
+  const int p = it.p;
+  const int hk = h / (prm.Hq / prm.Hkv);
+  int NB = 0;
+  if (unit_ok)
+    for (int ki = 0; ki < it.n_kv; ++ki) NB += kblocks(__ldg(prm.kv_list + it.kv_off + ki), p, prm.causal, prm.nb, qt);
+  auto block_at = [&](int j, int& kp, int& kbk) {
+    int r = j;
+    for (int ki = 0; ki < it.n_kv; ++ki) {
+      kp = __ldg(prm.kv_list + it.kv_off + ki);
+      const int n = kblocks(kp, p, prm.causal, prm.nb, qt);
+      if (r < n) {
+        kbk = r;
+        return;
+      }
+      r -= n;
+    }
+    kp = -1;
+    kbk = 0;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(Ly::B_QFULL), 1);
+    mbar_init(bar(Ly::B_KVFULL), 1);
+    mbar_init(bar(Ly::B_KVEMPTY), 1);
+    mbar_init(bar(Ly::B_SFULL), 1);
+    mbar_init(bar(Ly::B_PFULL), 4);  // one lane of each softmax warp
+    mbar_init(bar(Ly::B_OFULL), 1);
+    mbar_init(bar(Ly::B_DRAIN), 1);
+    *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0 || !unit_ok) ? 1 : 0;
+    if (!unit_ok) record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_ITEM, (int32_t)blockIdx.x);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(tmem_slot), 256);
+    tmem_relinquish();
+  }
+  if (warp == WARP_LOAD && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool run = *abort_flag == 0;
+  // TMEM columns: S [0, 64) (P pieces 0 and 1 packed into [0, 32) and [32, 64)), P piece 2
+  // packed into [64, 96), O [128, 128 + D)
+  constexpr uint32_t COL_PL = 64, COL_O = 128;
+
+  if (warp < 4) {
+    // ================================================================ softmax
+    const int row = warp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t tm_s = tmem + lane_base;
+    const uint32_t tm_pl = tmem + lane_base + COL_PL;
+    const uint32_t tm_o = tmem + lane_base + COL_O;
+    const int64_t q_local = (int64_t)qt * BM + row;
+    float m = -INFINITY, l = 0.f;
+    bool ok = run;
+    for (int j = 0; j < NB && ok; ++j) {
+      int kp, kbk;
+      block_at(j, kp, kbk);
+      // visible keys of this row in the block: [0, hi)
+      int hi = (int)min((int64_t)BN, L - (int64_t)kbk * BN);
+      if (prm.causal && kp == p) hi = (int)min((int64_t)hi, q_local - (int64_t)kbk * BN + 1);
+      ok = mbar_wait(bar(Ly::B_SFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_SOFTMAX, j);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float s[BN];
+      tmem_ld32(tm_s, s);
+      tmem_ld32(tm_s + 32u, s + 32);
+      tc_wait_ld();
+      float mb = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        s[c] = (c < hi) ? s[c] * prm.scale_log2 : -INFINITY;
+        mb = fmaxf(mb, s[c]);
+      }
+      const float m_new = fmaxf(m, mb);
+      const float mref = (m_new == -INFINITY) ? 0.f : m_new;
+      const float factor = (m == -INFINITY) ? 1.f : exp2f(m - mref);
+      m = m_new;
+      if (__any_sync(0xffffffffu, factor != 1.f) && j > 0) {
+        // O holds every earlier PV product: S(j) was issued after PV(j-1)
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          float o[32];
+          tmem_ld32(tm_o + (uint32_t)c, o);
+          tc_wait_ld();
+          uint32_t w[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(o[e] * factor);
+          tmem_st32(tm_o + (uint32_t)c, w);
+        }
+      }
+      float sum = 0.f;
+      uint32_t p1[BN / 2], p2[BN / 2], p3[BN / 2];
+#pragma unroll
+      for (int c = 0; c < BN; c += 2) {
+        const float e0 = exp2f(s[c] - mref), e1 = exp2f(s[c + 1] - mref);
+        sum += e0 + e1;
+        // exact three-piece split of each probability
+        const __nv_bfloat162 a = __floats2bfloat162_rn(e0, e1);
+        const float r0 = e0 - __low2float(a), r1 = e1 - __high2float(a);
+        const __nv_bfloat162 bb = __floats2bfloat162_rn(r0, r1);
+        const __nv_bfloat162 cc = __floats2bfloat162_rn(r0 - __low2float(bb), r1 - __high2float(bb));
+        p1[c / 2] = *reinterpret_cast<const uint32_t*>(&a);
+        p2[c / 2] = *reinterpret_cast<const uint32_t*>(&bb);
+        p3[c / 2] = *reinterpret_cast<const uint32_t*>(&cc);
+      }
+      l = l * factor + sum;
+      tmem_st32(tm_s, p1);
+      tmem_st32(tm_s + 32u, p2);
+      tmem_st32(tm_pl, p3);
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Ly::B_PFULL));
+    }
+    if (ok) {
+      ok = mbar_wait(bar(Ly::B_OFULL), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_SOFTMAX, -1);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int64_t prow = (((int64_t)b * prm.Hq + h) * prm.n_slots + it.slot) * L + q_local;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        float o[32];
+        tmem_ld32(tm_o + (uint32_t)c, o);
+        tc_wait_ld();
+        if (q_local < L) {
+          float4* dst = reinterpret_cast<float4*>(prm.part_o + prow * D + c);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
+        }
+      }
+      if (q_local < L) prm.part_lse[prow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    }
+  } else if (warp == WARP_MMA) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
+    const uint64_t q0 = smem_desc_sw128(sb + Ly::Q_OFF, 16u, 1024u);
+    const uint64_t k0 = smem_desc_sw128(sb + Ly::K_OFF, 16u, 1024u);
+    const uint64_t v0 = smem_desc_sw128(sb + Ly::V_OFF, Ly::KBOX, 1024u);
+    // K-major operand made of 64-column SW128 boxes: K-step kk sits in box kk/4 at byte 32 (kk % 4)
+    auto qoff = [](int kk) { return (uint64_t)((kk >> 2) * (Ly::QBOX >> 4) + (kk & 3) * 2); };
+    auto koff = [](int kk) { return (uint64_t)((kk >> 2) * (Ly::KBOX >> 4) + (kk & 3) * 2); };
+    const uint32_t p_col[3] = {0u, 32u, COL_PL};
+    bool ok = run && NB > 0;
+    if (ok) ok = mbar_wait_warp(bar(Ly::B_QFULL), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, -1);
+    for (int j = 0; j < NB && ok; ++j) {
+      ok = mbar_wait_warp(bar(Ly::B_KVFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA,
+                          j);
+      if (!ok) break;
+      tc_fence_after();
+      // S = Q K^T over the six piece pairs
+      for (int pr = 0; pr < NPAIR; ++pr) {
+        const uint64_t qd = q0 + (uint64_t)pair_a(pr) * (Ly::QP >> 4);
+        const uint64_t kd = k0 + (uint64_t)pair_b(pr) * (Ly::KP >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_ss_warp(tmem, qd + qoff(kk), kd + koff(kk), idesc_qk, (pr > 0 || kk > 0) ? 1u : 0u);
+      }
+      tc_commit_warp(bar(Ly::B_SFULL));
+      ok = mbar_wait_warp(bar(Ly::B_PFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
+      if (!ok) break;
+      tc_fence_after();
+      // O += P V over the six piece pairs; P's pieces from TMEM, V's MN-major from shared memory
+      for (int pr = 0; pr < NPAIR; ++pr) {
+        const uint32_t pa = tmem + p_col[pair_a(pr)];
+        const uint64_t vd = v0 + (uint64_t)pair_b(pr) * (Ly::KP >> 4);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          tc_mma_ts_warp(tmem + COL_O, pa + (uint32_t)(kk * 8), vd + (uint64_t)(kk * 128), idesc_pv,
+                         (j > 0 || pr > 0 || kk > 0) ? 1u : 0u);
+      }
+      tc_commit_warp(bar(Ly::B_KVEMPTY));  // K(j), V(j) free once these products complete
+    }
+    if (ok) tc_commit_warp(bar(Ly::B_OFULL));
+    tc_commit_warp(bar(Ly::B_DRAIN));
+    mbar_drain(bar(Ly::B_DRAIN), 0u, DRAIN_NS);
+  } else if (warp == WARP_LOAD && lane == 0) {
+    // ================================================================ producer
+    bool ok = run && NB > 0;
+    int issued = 0;
+    if (ok) {
+      const int64_t qrow = ((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + (int64_t)qt * BM;
+      mbar_expect_tx(bar(Ly::B_QFULL), 3 * Ly::QP);
+      for (int a = 0; a < 3; ++a)
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(sb + Ly::Q_OFF + (uint32_t)a * Ly::QP + (uint32_t)c * Ly::QBOX, &tmQ, c * 64,
+                      (int32_t)(qrow + (int64_t)a * prm.q_rows), bar(Ly::B_QFULL));
+    }
+    const int64_t kvbase = ((int64_t)b * prm.Hkv + hk) * prm.S;
+    for (int j = 0; j < NB && ok; ++j) {
+      if (j > 0) {
+        ok = mbar_wait(bar(Ly::B_KVEMPTY), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                       ROLE_LOAD, j);
+        if (!ok) break;
+      }
+      int kp, kbk;
+      block_at(j, kp, kbk);
+      if (kp < 0 || kp >= prm.P) {
+        record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_LOAD, (int32_t)blockIdx.x);
+        *abort_flag = 1;
+        break;
+      }
+      const int64_t krow = kvbase + (int64_t)kp * L + (int64_t)kbk * BN;
+      mbar_expect_tx(bar(Ly::B_KVFULL), 6 * Ly::KP);
+      for (int a = 0; a < 3; ++a)
+        for (int c = 0; c < D / 64; ++c) {
+          const int32_t y = (int32_t)(krow + (int64_t)a * prm.kv_rows);
+          tma_load_2d(sb + Ly::K_OFF + (uint32_t)a * Ly::KP + (uint32_t)c * Ly::KBOX, &tmK, c * 64, y,
+                      bar(Ly::B_KVFULL));
+          tma_load_2d(sb + Ly::V_OFF + (uint32_t)a * Ly::KP + (uint32_t)c * Ly::KBOX, &tmV, c * 64, y,
+                      bar(Ly::B_KVFULL));
+        }
+      ++issued;
+    }
+    if (run && NB > 0) mbar_drain(bar(Ly::B_QFULL), 0u, DRAIN_NS);
+    if (issued > 0) mbar_drain(bar(Ly::B_KVFULL), (uint32_t)((issued - 1) & 1), DRAIN_NS);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// fp32 rows -> three bf16 pieces [3][n][...] (x1 = bf16(x), x2 = bf16(x - x1), x3 = bf16(x - x1 - x2))
+__global__ void __launch_bounds__(256) split_kernel(const float4* __restrict__ x, uint2* __restrict__ out,
+                                                    int64_t n4, int32_t* status) {
+  if (*reinterpret_cast<volatile int32_t*>(status) != 0) return;
+  const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  if (i >= n4) return;
+  const float4 v = __ldcs(x + i);
+  const float e[4] = {v.x, v.y, v.z, v.w};
+  uint32_t w[3][2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(e[2 * h], e[2 * h + 1]);
+    const float r0 = e[2 * h] - __low2float(a), r1 = e[2 * h + 1] - __high2float(a);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(r0, r1);
+    const __nv_bfloat162 c = __floats2bfloat162_rn(r0 - __low2float(b), r1 - __high2float(b));
+    w[0][h] = *reinterpret_cast<const uint32_t*>(&a);
+    w[1][h] = *reinterpret_cast<const uint32_t*>(&b);
+    w[2][h] = *reinterpret_cast<const uint32_t*>(&c);
+  }
+#pragma unroll
+  for (int a = 0; a < 3; ++a) out[(int64_t)a * n4 + i] = make_uint2(w[a][0], w[a][1]);
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode(std::string* err) {
+  static EncodeTiledFn fn = nullptr;
+  if (fn) return fn;
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !ptr) {
+    *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return nullptr;
+  }
+  fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  return fn;
+}
+
+// [rows, d] bf16 row-major pieces, boxes of box_rows x 64 columns with 128-byte swizzle.
+static bool make_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, uint64_t rows, int d, int box_rows,
+                     std::string* err) {
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *err = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
+    return false;
+  }
+  return true;
+}
+
+static int split(const float* x, void* out, int64_t n, int32_t* status, cudaStream_t st, std::string* err) {
+  const int64_t n4 = n / 4;
+  if (n4 <= 0) return (int)cudaSuccess;
+  const int64_t blocks = (n4 + 255) / 256;
+  if (blocks > 0x7fffffff) {
+    *err = "tensor too large to split in one launch";
+    return (int)cudaErrorInvalidConfiguration;
+  }
+  split_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(x), static_cast<uint2*>(out), n4,
+                                                 status);
+  return (int)cudaGetLastError();
+}
+
+template <int D>
+static int launch(const TileArgs& a, void* stream, std::string* err) {
+  const int64_t nqt = (a.L + BM - 1) / BM;
+  const int64_t nb = (a.L + BN - 1) / BN;
+  const int64_t units = (int64_t)a.n_items * a.B * a.Hq * nqt;
+  if (units <= 0) return (int)cudaSuccess;
+  const int64_t q_rows = (int64_t)a.B * a.Hq * a.S, kv_rows = (int64_t)a.B * a.Hkv * a.S;
+  if (units > 0x7fffffff || 3 * q_rows >= ((int64_t)1 << 31) || 3 * kv_rows >= ((int64_t)1 << 31)) {
+    *err = "fp32 tensor-core path: too many rows or work units for one launch";
+    return (int)cudaErrorInvalidConfiguration;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  const F32Pieces pc = f32_pieces_layout(a.B, a.Hq, a.Hkv, a.S, a.d);
+  char* base = static_cast<char*>(a.pieces);
+  int ce = split(static_cast<const float*>(a.Q), base + pc.q_off, q_rows * D, a.status, st, err);
+  if (ce == (int)cudaSuccess) ce = split(static_cast<const float*>(a.K), base + pc.k_off, kv_rows * D, a.status, st, err);
+  if (ce == (int)cudaSuccess) ce = split(static_cast<const float*>(a.V), base + pc.v_off, kv_rows * D, a.status, st, err);
+  if (ce != (int)cudaSuccess) {
+    if (err->empty()) *err = std::string("split launch: ") + cudaGetErrorString((cudaError_t)ce);
+    return ce;
+  }
+  EncodeTiledFn enc = get_encode(err);
+  if (!enc) return (int)cudaErrorNotSupported;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(enc, &mq, base + pc.q_off, (uint64_t)(3 * q_rows), D, BM, err) ||
+      !make_map(enc, &mk, base + pc.k_off, (uint64_t)(3 * kv_rows), D, BN, err) ||
+      !make_map(enc, &mv, base + pc.v_off, (uint64_t)(3 * kv_rows), D, BN, err))
+    return (int)cudaErrorInvalidValue;
+  Params prm;
+  prm.items = a.items;
+  prm.kv_list = a.kv_list;
+  prm.part_o = a.part_o;
+  prm.part_lse = a.part_lse;
+  prm.status = a.status;
+  prm.S = a.S;
+  prm.L = a.L;
+  prm.q_rows = q_rows;
+  prm.kv_rows = kv_rows;
+  prm.B = a.B;
+  prm.Hq = a.Hq;
+  prm.Hkv = a.Hkv;
+  prm.P = a.P;
+  prm.n_items = a.n_items;
+  prm.n_slots = a.n_slots;
+  prm.nqt = (int32_t)nqt;
+  prm.nb = (int32_t)nb;
+  prm.causal = a.causal;
+  prm.scale_log2 = a.scale_log2;
+  prm.wait_limit_ns = a.wait_limit_ns;
+  auto kern = tile_fwd_tc32_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<D>::TOTAL);
+  if (e != cudaSuccess) {
+    *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+    return (int)e;
+  }
+  kern<<<dim3((unsigned)units), dim3(NUM_THREADS), Layout<D>::TOTAL, st>>>(mq, mk, mv, prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) *err = std::string("tile_fwd_tc32 launch: ") + cudaGetErrorString(e);
+  return (int)e;
+}
+
+}  // namespace tc32
+
+F32Pieces f32_pieces_layout(int32_t B, int32_t Hq, int32_t Hkv, int64_t S, int32_t d) {
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  F32Pieces p{};
+  const size_t qb = (size_t)3 * B * Hq * (size_t)S * d * 2, kvb = (size_t)3 * B * Hkv * (size_t)S * d * 2;
+  p.q_off = 0;
+  p.k_off = up(qb);
+  p.v_off = p.k_off + up(kvb);
+  p.total = p.v_off + up(kvb);
+  return p;
+}
+
+int launch_tile_fwd_tc32(const TileArgs& a, void* stream, std::string* err) {
+  if (a.d == 128) return tc32::launch<128>(a, stream, err);
+  if (a.d == 64) return tc32::launch<64>(a, stream, err);
+  *err = "fp32 tensor-core tile kernel supports d = 64 or 128";
+  return (int)cudaErrorInvalidValue;
+}
+
+}  // namespace mesh
