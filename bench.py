@@ -343,6 +343,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
+    ap.add_argument("--wait-limit-ns", type=int, default=None,
+                    help="bound on every device-side wait (default 2e9); raise it for runs under a profiler, "
+                         "whose replay passes can slow a kernel by orders of magnitude")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
@@ -350,6 +353,8 @@ def main():
 
     import tiled_distributed_attention_gb300 as m
     m.load_library()
+    if args.wait_limit_ns is not None:
+        m.mesh_attn_set_wait_limit_ns(args.wait_limit_ns)
     ws, rank, local = dist_env()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)

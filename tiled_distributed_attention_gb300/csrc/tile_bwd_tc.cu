@@ -534,8 +534,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar(Ly::B_S), 1);
     mbar_init(bar(Ly::B_S + 1), 1);
     mbar_init(bar(Ly::B_DP), 1);
-    mbar_init(bar(Ly::B_P), N_EW);
-    mbar_init(bar(Ly::B_DS), N_EW);
+    mbar_init(bar(Ly::B_DS), N_EW);  // one lane of each elementwise warp
     mbar_init(bar(Ly::B_ACC), 1);
     mbar_init(bar(Ly::B_DRAIN), 1);
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0 || !unit_ok) ? 1 : 0;
@@ -607,10 +606,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tmem_ld32(tm_s + (uint32_t)c_base, pv);
       tmem_ld32(tm_s + (uint32_t)c_base + 32u, pv + 32);
       tc_wait_ld();
-      // the S buffer is free once read: tell the MMA issuer (it may compute S(j+2) into it)
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(Ly::B_P));
       if (any_mask) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
@@ -730,10 +725,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     for (int j = 0; j < NB && ok; ++j) {
-      // S(j) has been read (its buffer is free for S(j+2)) and dS(j) is in TMEM
-      ok = mbar_wait_warp(bar(Ly::B_P), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
-      if (ok)
-        ok = mbar_wait_warp(bar(Ly::B_DS), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
+      // dS(j) is in TMEM, and S(j) has been read, so its buffer is free for S(j+2).  (One barrier per
+      // block, passed in order: a second "S read" barrier could complete for block j+1, whose S is
+      // issued two blocks ahead, before this warp observed block j -- two phases ahead of its
+      // parity wait.)
+      ok = mbar_wait_warp(bar(Ly::B_DS), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
       if (!ok) break;
       tc_fence_after();
       issue_dq(j % Ly::NSA, j == 0);
