@@ -103,6 +103,74 @@ __device__ __forceinline__ int kblocks_of(int k, int p, int causal, int nb, int 
 // query blocks of partition `p` visited by key block `kb` of partition `k` (dkdv kernel)
 __device__ __forceinline__ int qblock_begin(int k, int p, int causal, int kb) { return (causal && k == p) ? kb : 0; }
 
+// Row stride (floats) of a warp's 32 x 32 staging chunk: 36 keeps both the row-wise writes and
+// the column-wise reads below free of bank conflicts.
+constexpr int STG_LD = 36;
+
+// Store one warp's 32 x 32 fp32 chunk -- lane r holds columns [c, c + 32) of row row0 + r, times
+// `mul` -- into a row-major [rows][D] buffer.  The chunk goes through shared memory so that each
+// store instruction writes four whole 128-byte row segments instead of 32 scattered 16-byte
+// pieces.  Rows from `rows_valid` on are not written.
+template <int D>
+__device__ __forceinline__ void store_rows(float* stg, const float (&v)[32], float mul, float* dst, int64_t row0,
+                                           int rows_valid, int c, int lane) {
+  float4* mine = reinterpret_cast<float4*>(stg + lane * STG_LD);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) mine[e] = make_float4(v[4 * e] * mul, v[4 * e + 1] * mul, v[4 * e + 2] * mul, v[4 * e + 3] * mul);
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const int rr = 4 * r + (lane >> 3);
+    const float4 x = *reinterpret_cast<const float4*>(stg + rr * STG_LD + (lane & 7) * 4);
+    if (rr < rows_valid) *reinterpret_cast<float4*>(dst + (row0 + rr) * D + c + (lane & 7) * 4) = x;
+  }
+  __syncwarp();
+}
+
+// Walk over the key blocks of a dq unit in the order the producer loads them: the tile's KV
+// partitions, then the partition's blocks (on the causal diagonal only up to the query block).
+struct KCursor {
+  int ki, kp, kb, n;
+  __device__ __forceinline__ void load(const Params& prm, const DevItem& it, int p, int qb) {
+    kp = __ldg(prm.kv_list + it.kv_off + ki);
+    kb = 0;
+    n = kblocks_of(kp, p, prm.causal, prm.nb, qb);
+  }
+  __device__ __forceinline__ void start(const Params& prm, const DevItem& it, int p, int qb) {
+    ki = 0;
+    load(prm, it, p, qb);
+  }
+  __device__ __forceinline__ void step(const Params& prm, const DevItem& it, int p, int qb) {
+    if (++kb < n) return;
+    ++ki;
+    if (ki < it.n_kv) load(prm, it, p, qb);
+    else kp = -1;
+  }
+};
+
+// Walk over the query blocks of a dkdv unit in the order the producer loads them: heads of the
+// group, then the slot's Q partitions, then the partition's blocks.
+struct QCursor {
+  int h, qi, p, qb;
+  __device__ __forceinline__ void load(const Params& prm, const DevItem& it, int k, int kb) {
+    p = __ldg(prm.q_list + it.kv_off + qi);
+    qb = qblock_begin(k, p, prm.causal, kb);
+  }
+  __device__ __forceinline__ void start(const Params& prm, const DevItem& it, int k, int kb, int h0) {
+    h = h0;
+    qi = 0;
+    load(prm, it, k, kb);
+  }
+  __device__ __forceinline__ void step(const Params& prm, const DevItem& it, int k, int kb) {
+    if (++qb < prm.nb) return;
+    if (++qi >= it.n_kv) {
+      qi = 0;
+      ++h;
+    }
+    load(prm, it, k, kb);
+  }
+};
+
 // Descriptor offsets (16-byte units) of a 128-row operand made of 64-column SW128 boxes.
 template <int D>
 __device__ __forceinline__ uint64_t kmaj_off(int kk) {
@@ -116,6 +184,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                     const Params prm) {
   using Ly = Layout<D>;
+  static_assert(Ly::NSA * Ly::TILE >= N_EW * 32 * STG_LD * 4, "epilogue staging must fit the stream stages");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sb = smem_u32(smem_raw);
   if (sb & 1023u) {  // 128-byte swizzle atoms need 1024-aligned operands (see Layout)
@@ -219,41 +288,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tm_dp = tmem + lane_base + 128u;   // dP^T, then dS^T (bf16)
     const uint32_t tm_dv = tmem + lane_base + 256u;
     const uint32_t tm_dk = tmem + lane_base + 256u + (uint32_t)D;
-    const int64_t key_local = (int64_t)kb * BM + row;
     bool ok = run;
-    // -LSE log2 e / -D of query column `row`, loaded one block ahead by the first column half
-    float nxt_lse = 0.f, nxt_d = 0.f;
-    auto fetch = [&](int i) {
-      int h, p, qb;
-      block_at(i, h, p, qb);
-      const int64_t ql = (int64_t)qb * BM + row;
-      if (p >= 0 && p < prm.P && ql < L) {
-        const int64_t gi = ((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + ql;
-        nxt_lse = -__ldg(prm.lse + gi) * LOG2E;
-        nxt_d = -__ldg(prm.dsum + gi);
-      } else {
-        nxt_lse = -INFINITY;  // no such query row: exp2(s - inf) = 0, so it needs no mask
-        nxt_d = 0.f;
+    // Query-block cursors: `cur` is block i, `nxt` block i + 1.  Stepping them keeps the global
+    // reads of the slot's partition list off the per-block path (one read per partition change).
+    QCursor cur, nxt;
+    cur.start(prm, it, k, kb, hk * g);
+    nxt = cur;
+    // LSE and D of query column `row` for the next block, loaded raw one block ahead by the first
+    // column half and only used (scaled, published) at the top of the next iteration, so that the
+    // loads never stall the block in flight
+    float raw_lse = 0.f, raw_d = 0.f;
+    bool raw_in = false;
+    auto fetch = [&](const QCursor& c) {
+      const int64_t ql = (int64_t)c.qb * BM + row;
+      raw_in = c.p >= 0 && c.p < prm.P && ql < L;
+      if (raw_in) {
+        const int64_t gi = ((int64_t)b * prm.Hq + c.h) * prm.S + (int64_t)c.p * L + ql;
+        raw_lse = __ldg(prm.lse + gi);
+        raw_d = __ldg(prm.dsum + gi);
       }
     };
-    if (ok && NBQ > 0 && hf == 0) fetch(0);
+    if (ok && NBQ > 0 && hf == 0) fetch(cur);
     for (int i = 0; i < NBQ && ok; ++i) {
       const int vb = i & 1;
+      if (i > 0) cur = nxt;
+      if (i + 1 < NBQ) nxt.step(prm, it, k, kb);
       // publish this column's values, then wait (bounded) until all 128 columns are written; a
       // buffer is rewritten two blocks later, after every writer has arrived for the block between
       if (hf == 0) {
-        nlse_s[vb * BM + row] = nxt_lse;
-        ndsum_s[vb * BM + row] = nxt_d;
+        // no such query row: exp2(s - inf) = 0, so it needs no mask
+        nlse_s[vb * BM + row] = raw_in ? -raw_lse * LOG2E : -INFINITY;
+        ndsum_s[vb * BM + row] = raw_in ? -raw_d : 0.f;
         mbar_arrive(bar(Ly::B_VEC + vb));
-        if (i + 1 < NBQ) fetch(i + 1);
+        if (i + 1 < NBQ) fetch(nxt);
       }
       ok = mbar_wait(bar(Ly::B_VEC + vb), (uint32_t)((i >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
                      ROLE_EW, i);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      int h, p, qb;
-      block_at(i, h, p, qb);
-      (void)h;
+      const int p = cur.p, qb = cur.qb;
       // causal diagonal block: query columns before this key row are masked (query rows past the
       // partition end carry -inf in place of -LSE and need no mask)
       const int lo = (prm.causal && p == k && qb == kb) ? row - c_base : 0;
@@ -326,23 +399,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (ok) {
       tc_fence_after();
-      const int64_t prow = (((int64_t)b * prm.Hkv + hk) * prm.n_kv_slots + it.slot) * L + key_local;
+      // the stream stages are idle once every product has completed: stage the rows there
+      float* stg = reinterpret_cast<float*>(smem + Ly::A0) + warp * (32 * STG_LD);
+      const int64_t row0 = (((int64_t)b * prm.Hkv + hk) * prm.n_kv_slots + it.slot) * L + (int64_t)kb * BM + wq * 32;
+      const int rows_valid = (int)max((int64_t)0, min((int64_t)32, L - ((int64_t)kb * BM + wq * 32)));
 #pragma unroll 1
       for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
-        float v[32], kk[32];
+        float v[32];
         tmem_ld32(tm_dv + (uint32_t)c, v);
-        tmem_ld32(tm_dk + (uint32_t)c, kk);
         tc_wait_ld();
-        if (key_local < L) {
-          float4* dvp = reinterpret_cast<float4*>(prm.dv_part + prow * D + c);
-          float4* dkp = reinterpret_cast<float4*>(prm.dk_part + prow * D + c);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            dvp[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-            dkp[e] = make_float4(kk[4 * e] * prm.scale, kk[4 * e + 1] * prm.scale, kk[4 * e + 2] * prm.scale,
-                                 kk[4 * e + 3] * prm.scale);
-          }
-        }
+        store_rows<D>(stg, v, 1.f, prm.dv_part, row0, rows_valid, c, lane);
+        tmem_ld32(tm_dk + (uint32_t)c, v);
+        tc_wait_ld();
+        store_rows<D>(stg, v, prm.scale, prm.dk_part, row0, rows_valid, c, lane);
       }
     }
   } else if (warp == WARP_MMA) {
@@ -493,6 +562,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                   const Params prm) {
   using Ly = Layout<D>;
+  static_assert(Ly::NSA * Ly::TILE >= N_EW * 32 * STG_LD * 4, "epilogue staging must fit the stream stages");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sb = smem_u32(smem_raw);
   if (sb & 1023u) {  // 128-byte swizzle atoms need 1024-aligned operands (see Layout)
@@ -588,9 +658,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float lse2 = row_in ? __ldg(prm.lse + grow) * LOG2E : INFINITY;
     const float dsum = row_in ? __ldg(prm.dsum + grow) : 0.f;
     bool ok = run;
+    KCursor cur;
+    cur.start(prm, it, p, qb);
     for (int j = 0; j < NB && ok; ++j) {
-      int kp, kbk;
-      block_at(j, kp, kbk);
+      if (j > 0) cur.step(prm, it, p, qb);
+      const int kp = cur.kp, kbk = cur.kb;
       const int64_t kvalid = L - (int64_t)kbk * BM;
       int hi = (int)min((int64_t)BM, kvalid);                         // keys past the partition end
       if (prm.causal && kp == p && kbk == qb) hi = min(hi, row + 1);  // diagonal block
@@ -650,19 +722,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (ok) {
       tc_fence_after();
-      const int64_t prow = (((int64_t)b * prm.Hq + h) * prm.n_slots + it.slot) * L + q_local;
+      float* stg = reinterpret_cast<float*>(smem + Ly::A0) + warp * (32 * STG_LD);  // idle K stages
+      const int64_t row0 = (((int64_t)b * prm.Hq + h) * prm.n_slots + it.slot) * L + (int64_t)qb * BM + wq * 32;
+      const int rows_valid = (int)max((int64_t)0, min((int64_t)32, L - ((int64_t)qb * BM + wq * 32)));
 #pragma unroll 1
       for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
         float v[32];
         tmem_ld32(tm_dq + (uint32_t)c, v);
         tc_wait_ld();
-        if (row_in) {
-          float4* dst = reinterpret_cast<float4*>(prm.dq_part + prow * D + c);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(v[4 * e] * prm.scale, v[4 * e + 1] * prm.scale, v[4 * e + 2] * prm.scale,
-                                 v[4 * e + 3] * prm.scale);
-        }
+        store_rows<D>(stg, v, prm.scale, prm.dq_part, row0, rows_valid, c, lane);
       }
     }
   } else if (warp == WARP_MMA) {
