@@ -456,19 +456,31 @@ def main():
         # counters only describe the kernel they were taken on
         if rec and sha.startswith(rec["source_sha256_prefix"]):
             traffic = rec["bytes"]
+    if w.dtype == "bf16":
+        roof = {"bound": "tensor", "achieved": tile_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": tile_tflops / peaks["bf16_tflops"], "traffic": traffic,
+                "kernel": "tile_fwd_tc_kernel", "peak_kind": f"{peak_kind} bf16 dense burst"}
+        launches_per_step = 2  # tile, merge
+    else:
+        # fp32 inputs: every product is six bf16 tensor-core products of the operands' exact
+        # three-piece split, so the ceiling for the fp32 rate is the bf16 peak / 6
+        peak32 = peaks["bf16_tflops"] / 6
+        roof = {"bound": "tensor", "achieved": tile_tflops, "peak": peak32, "unit": "TFLOP/s",
+                "frac": tile_tflops / peak32, "traffic": None,
+                "kernel": "split_kernel + tile_fwd_tc32_kernel",
+                "peak_kind": f"{peak_kind} bf16 dense burst / 6 (six bf16 products per fp32 product)"}
+        launches_per_step = 3  # split, tile, merge
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": workload_config(w, args.plan),
-        "roofline": {"bound": "tensor", "achieved": tile_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": tile_tflops / peaks["bf16_tflops"], "traffic": traffic,
-                     "kernel": "tile_fwd_tc_kernel", "peak_kind": f"{peak_kind} bf16 dense burst"},
+        "roofline": roof,
         "merge": {"bound": "hbm", "achieved": merge_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                   "frac": merge_gbs / peaks["hbm_gbs"], "bytes_per_launch": mbytes, "ms": merge_ms},
         "tile_fwd_ms": tile_ms, "merge_ms": merge_ms, "backward": bwd,
         "comm_counted": counted_volumes(m, w),
-        "cpu_baseline": cpu_base, "e2e": e2e, "gpu_launches": 2 * args.steps,
+        "cpu_baseline": cpu_base, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
