@@ -221,3 +221,27 @@ def test_backward_full_size(lib, name):
     print(f"[parity-bwd] {name} sampled dQ rows: max|err| = {e.max().item():.3e}, "
           f"max err/bound = {(e / bound).max().item():.3f}")
     assert (e <= bound).all()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("shape", [(1, 1, 1), (1, 3, 37), (2, 5, 301)], ids=["one_row", "rows111", "rows3010"])
+def test_prep_row_sums(lib, dtype, d, shape):
+    """D_i = dO_i . O_i from the prep call against the fp64 sum over the same stored values, for
+    row counts that leave every CTA shape ragged.  fp32 accumulation of d products: within
+    d 2^-24 sum |dO O| (taken as 1e-5 sum |dO O| + 1e-7)."""
+    B, H, S = shape
+    g = torch.Generator().manual_seed(7000 + d + S)
+    O = torch.randn(B, H, S, d, generator=g).to(dtype)
+    dO = torch.randn(B, H, S, d, generator=g).to(dtype)
+    D = torch.full((B, H, S), float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    lib.mesh_attn_bwd_prep(O.cuda(), dO.cuda(), D, status)
+    torch.cuda.synchronize()
+    assert status.cpu().tolist() == [0, 0, 0, 0]
+    prod = O.double() * dO.double()
+    ref = prod.sum(dim=-1)
+    tol = 1e-5 * prod.abs().sum(dim=-1) + 1e-7
+    err = (D.double().cpu() - ref).abs()
+    assert torch.isfinite(D).all()
+    assert (err <= tol).all(), err.max().item()

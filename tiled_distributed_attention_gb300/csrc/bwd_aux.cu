@@ -18,20 +18,6 @@ namespace mesh {
 namespace baux {
 
 template <typename T>
-__device__ __forceinline__ float4 load4(const T* p);
-template <>
-__device__ __forceinline__ float4 load4<float>(const float* p) {
-  return __ldcs(reinterpret_cast<const float4*>(p));
-}
-template <>
-__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
-  const uint2 w = __ldcs(reinterpret_cast<const uint2*>(p));
-  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
-  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
-  return make_float4(a.x, a.y, b.x, b.y);
-}
-
-template <typename T>
 __device__ __forceinline__ void store4(T* o, float4 v);
 template <>
 __device__ __forceinline__ void store4<float>(float* o, float4 v) {
@@ -47,25 +33,75 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* o, float4 v
   *reinterpret_cast<uint2*>(o) = w;
 }
 
-// One warp per row, 8 rows per CTA of 256 threads; each lane reads D/32 consecutive elements
-// (4 per 16-byte or 8-byte load) of O and dO.
+// 16 bytes of a row as floats: 8 bf16 or 4 fp32 elements.
+template <typename T>
+struct Vec16;
+template <>
+struct Vec16<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void load(const float* p, float* out) {
+    const float4 v = __ldcs(reinterpret_cast<const float4*>(p));
+    out[0] = v.x, out[1] = v.y, out[2] = v.z, out[3] = v.w;
+  }
+};
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void load(const __nv_bfloat16* p, float* out) {
+    const uint4 w = __ldcs(reinterpret_cast<const uint4*>(p));
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[i]));
+      out[2 * i] = f.x, out[2 * i + 1] = f.y;
+    }
+  }
+};
+
+// A row is read by LPR = D / (16 / sizeof(T)) lanes with one 16-byte load each of O and dO; a
+// warp covers 32 / LPR rows per step and PREP_STEPS steps, all loads issued before the first
+// product, so that every thread keeps 2 PREP_STEPS 16-byte loads in flight.
+constexpr int PREP_STEPS = 4;
+template <typename T, int D>
+struct PrepShape {
+  static constexpr int LPR = D / Vec16<T>::N;        // lanes per row
+  static constexpr int RPS = 32 / LPR;               // rows per warp step
+  static constexpr int ROWS_PER_WARP = RPS * PREP_STEPS;
+  static constexpr int ROWS_PER_CTA = 8 * ROWS_PER_WARP;
+  static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "row must split evenly over the lanes");
+};
+
 template <typename T, int D>
 __global__ void __launch_bounds__(256) prep_kernel(const T* O, const T* dO, float* Dsum, int32_t* status,
                                                    int64_t rows) {
+  using Sh = PrepShape<T, D>;
+  constexpr int N = Vec16<T>::N;
   if (*reinterpret_cast<volatile int32_t*>(status) != 0) return;
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  float acc = 0.f;
+  const int sub = lane / Sh::LPR, col = (lane % Sh::LPR) * N;
+  const int64_t row0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * Sh::ROWS_PER_WARP + sub;
+  float o[PREP_STEPS][N], g[PREP_STEPS][N];
 #pragma unroll
-  for (int c = lane * 4; c < D; c += 128) {
-    const float4 o = load4<T>(O + row * D + c);
-    const float4 g = load4<T>(dO + row * D + c);
-    acc = fmaf(o.x, g.x, fmaf(o.y, g.y, fmaf(o.z, g.z, fmaf(o.w, g.w, acc))));
+  for (int st = 0; st < PREP_STEPS; ++st) {
+    const int64_t row = row0 + (int64_t)st * Sh::RPS;
+    if (row < rows) {
+      Vec16<T>::load(O + row * D + col, o[st]);
+      Vec16<T>::load(dO + row * D + col, g[st]);
+    }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) Dsum[row] = acc;
+  for (int st = 0; st < PREP_STEPS; ++st) {
+    const int64_t row = row0 + (int64_t)st * Sh::RPS;
+    float acc = 0.f;
+    if (row < rows) {
+#pragma unroll
+      for (int e = 0; e < N; ++e) acc = fmaf(o[st][e], g[st][e], acc);
+    }
+    // sum over the LPR lanes of the row (aligned groups of lanes)
+#pragma unroll
+    for (int off = Sh::LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && lane % Sh::LPR == 0) Dsum[row] = acc;
+  }
 }
 
 // One CTA of 256 threads per ROWS consecutive rows of one (batch, head, partition): its share of
@@ -120,7 +156,8 @@ __global__ void __launch_bounds__(256) reduce_kernel(const ReduceArgs a, int n_r
 template <typename T, int D>
 int launch_prep(const PrepArgs& a, void* stream, std::string* err) {
   const int64_t rows = (int64_t)a.B * a.H * a.S;
-  const int64_t blocks = (rows + 7) / 8;
+  constexpr int64_t per_cta = PrepShape<T, D>::ROWS_PER_CTA;
+  const int64_t blocks = (rows + per_cta - 1) / per_cta;
   if (blocks <= 0) return (int)cudaSuccess;
   if (blocks > 0x7fffffff) {
     *err = "too many rows for one launch";
