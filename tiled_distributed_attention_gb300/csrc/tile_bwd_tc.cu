@@ -103,28 +103,58 @@ __device__ __forceinline__ int kblocks_of(int k, int p, int causal, int nb, int 
 // query blocks of partition `p` visited by key block `kb` of partition `k` (dkdv kernel)
 __device__ __forceinline__ int qblock_begin(int k, int p, int causal, int kb) { return (causal && k == p) ? kb : 0; }
 
-// Row stride (floats) of a warp's 32 x 32 staging chunk: 36 keeps both the row-wise writes and
-// the column-wise reads below free of bank conflicts.
-constexpr int STG_LD = 36;
+__device__ __forceinline__ float4 shfl4(float4 x, int src) {
+  x.x = __shfl_sync(0xffffffffu, x.x, src);
+  x.y = __shfl_sync(0xffffffffu, x.y, src);
+  x.z = __shfl_sync(0xffffffffu, x.z, src);
+  x.w = __shfl_sync(0xffffffffu, x.w, src);
+  return x;
+}
 
 // Store one warp's 32 x 32 fp32 chunk -- lane r holds columns [c, c + 32) of row row0 + r, times
-// `mul` -- into a row-major [rows][D] buffer.  The chunk goes through shared memory so that each
-// store instruction writes four whole 128-byte row segments instead of 32 scattered 16-byte
-// pieces.  Rows from `rows_valid` on are not written.
+// `mul` -- into a row-major [rows][D] buffer.  Each group of four lanes transposes its 4 x 4
+// matrix of 16-byte pieces (two exchange steps: lanes ^ 2, then lanes ^ 1), after which lane
+// 4a + i holds piece i of rows 4a .. 4a + 3; so each store instruction writes eight 64-byte row
+// segments (whole sectors) instead of 32 scattered 16-byte pieces, without shared memory.  Rows
+// from `rows_valid` on are not written.
 template <int D>
-__device__ __forceinline__ void store_rows(float* stg, const float (&v)[32], float mul, float* dst, int64_t row0,
+__device__ __forceinline__ void store_rows(const float (&v)[32], float mul, float* dst, int64_t row0,
                                            int rows_valid, int c, int lane) {
-  float4* mine = reinterpret_cast<float4*>(stg + lane * STG_LD);
+  const int i = lane & 3, rbase = lane & ~3;
+  const bool hi = (i & 2) != 0, odd = (i & 1) != 0;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) mine[e] = make_float4(v[4 * e] * mul, v[4 * e + 1] * mul, v[4 * e + 2] * mul, v[4 * e + 3] * mul);
-  __syncwarp();
+  for (int blk = 0; blk < 2; ++blk) {
+    float4 e[4];
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    const int rr = 4 * r + (lane >> 3);
-    const float4 x = *reinterpret_cast<const float4*>(stg + rr * STG_LD + (lane & 7) * 4);
-    if (rr < rows_valid) *reinterpret_cast<float4*>(dst + (row0 + rr) * D + c + (lane & 7) * 4) = x;
+    for (int q = 0; q < 4; ++q) {
+      const int o = 16 * blk + 4 * q;
+      e[q] = make_float4(v[o] * mul, v[o + 1] * mul, v[o + 2] * mul, v[o + 3] * mul);
+    }
+    {  // swap the off-diagonal 2 x 2 blocks with lane ^ 2
+      const float4 r0 = shfl4(hi ? e[0] : e[2], lane ^ 2), r1 = shfl4(hi ? e[1] : e[3], lane ^ 2);
+      if (hi) {
+        e[0] = r0;
+        e[1] = r1;
+      } else {
+        e[2] = r0;
+        e[3] = r1;
+      }
+    }
+    {  // swap within the 2 x 2 blocks with lane ^ 1
+      const float4 r0 = shfl4(odd ? e[0] : e[1], lane ^ 1), r1 = shfl4(odd ? e[2] : e[3], lane ^ 1);
+      if (odd) {
+        e[0] = r0;
+        e[2] = r1;
+      } else {
+        e[1] = r0;
+        e[3] = r1;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (rbase + j < rows_valid)
+        *reinterpret_cast<float4*>(dst + (row0 + rbase + j) * D + c + 16 * blk + 4 * i) = e[j];
   }
-  __syncwarp();
 }
 
 // Walk over the key blocks of a dq unit in the order the producer loads them: the tile's KV
@@ -184,7 +214,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                     const Params prm) {
   using Ly = Layout<D>;
-  static_assert(Ly::NSA * Ly::TILE >= N_EW * 32 * STG_LD * 4, "epilogue staging must fit the stream stages");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sb = smem_u32(smem_raw);
   if (sb & 1023u) {  // 128-byte swizzle atoms need 1024-aligned operands (see Layout)
@@ -399,8 +428,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (ok) {
       tc_fence_after();
-      // the stream stages are idle once every product has completed: stage the rows there
-      float* stg = reinterpret_cast<float*>(smem + Ly::A0) + warp * (32 * STG_LD);
       const int64_t row0 = (((int64_t)b * prm.Hkv + hk) * prm.n_kv_slots + it.slot) * L + (int64_t)kb * BM + wq * 32;
       const int rows_valid = (int)max((int64_t)0, min((int64_t)32, L - ((int64_t)kb * BM + wq * 32)));
 #pragma unroll 1
@@ -408,10 +435,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float v[32];
         tmem_ld32(tm_dv + (uint32_t)c, v);
         tc_wait_ld();
-        store_rows<D>(stg, v, 1.f, prm.dv_part, row0, rows_valid, c, lane);
+        store_rows<D>(v, 1.f, prm.dv_part, row0, rows_valid, c, lane);
         tmem_ld32(tm_dk + (uint32_t)c, v);
         tc_wait_ld();
-        store_rows<D>(stg, v, prm.scale, prm.dk_part, row0, rows_valid, c, lane);
+        store_rows<D>(v, prm.scale, prm.dk_part, row0, rows_valid, c, lane);
       }
     }
   } else if (warp == WARP_MMA) {
@@ -562,7 +589,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                   const Params prm) {
   using Ly = Layout<D>;
-  static_assert(Ly::NSA * Ly::TILE >= N_EW * 32 * STG_LD * 4, "epilogue staging must fit the stream stages");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sb = smem_u32(smem_raw);
   if (sb & 1023u) {  // 128-byte swizzle atoms need 1024-aligned operands (see Layout)
@@ -722,7 +748,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if (ok) {
       tc_fence_after();
-      float* stg = reinterpret_cast<float*>(smem + Ly::A0) + warp * (32 * STG_LD);  // idle K stages
       const int64_t row0 = (((int64_t)b * prm.Hq + h) * prm.n_slots + it.slot) * L + (int64_t)qb * BM + wq * 32;
       const int rows_valid = (int)max((int64_t)0, min((int64_t)32, L - ((int64_t)qb * BM + wq * 32)));
 #pragma unroll 1
@@ -730,7 +755,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float v[32];
         tmem_ld32(tm_dq + (uint32_t)c, v);
         tc_wait_ld();
-        store_rows<D>(stg, v, prm.scale, prm.dq_part, row0, rows_valid, c, lane);
+        store_rows<D>(v, prm.scale, prm.dq_part, row0, rows_valid, c, lane);
       }
     }
   } else if (warp == WARP_MMA) {
