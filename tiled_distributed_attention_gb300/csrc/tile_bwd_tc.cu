@@ -33,6 +33,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <string>
 
 #include "internal.h"
@@ -66,8 +67,11 @@ struct Params {
   float* dk_part;
   float* dv_part;
   int32_t* status;
+  uint32_t* counter_dq;  // unit counters of the two kernels, 0 at launch
+  uint32_t* counter_kv;
   int64_t S, L;
   int32_t B, Hq, Hkv, P, n_items, n_slots, n_kv_items, n_kv_slots, nb, causal;
+  int32_t n_dq_units, n_kv_units;
   float scale, scale_log2;
   int64_t wait_limit_ns;
 };
@@ -89,9 +93,11 @@ struct Layout {
   static constexpr uint32_t BAR_OFF = VEC_OFF + 4 * BM * 4;
   static constexpr int B_RES = 0, B_AF = 1, B_AE = B_AF + NSA, B_BF = B_AE + NSA, B_BE = B_BF + NSB,
                        B_S = B_BE + NSB, B_DP = B_S + 2, B_P = B_DP + 1, B_DS = B_P + 1, B_ACC = B_DS + 1,
-                       B_DRAIN = B_ACC + 1, B_VEC = B_DRAIN + 1, NBARS = B_VEC + 2;
+                       B_DRAIN = B_ACC + 1, B_VEC = B_DRAIN + 1, B_RESE = B_VEC + 2, B_ACCE = B_RESE + 1,
+                       B_UF = B_ACCE + 1, B_UE = B_UF + 2, NBARS = B_UE + 2;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag
-  static constexpr uint32_t TOTAL = MISC_OFF + 16;
+  static constexpr uint32_t RING_OFF = MISC_OFF + 16;         // unit ring: 2 decoded units, 16 ints each
+  static constexpr uint32_t TOTAL = RING_OFF + 2 * 64;
   static constexpr uint32_t ALLOC = TOTAL;
 };
 
@@ -208,6 +214,45 @@ __device__ __forceinline__ uint64_t kmaj_off(int kk) {
 }
 
 // ================================================================== dK / dV
+// unit -> (KV slot, batch, KV head, 128-key block), key block fastest
+struct KvUnit {
+  int kb, hk, b, NBQ;
+  DevItem it;  // {k, kv slot, q_off, n_q}
+  bool ok;
+};
+__device__ __forceinline__ KvUnit kv_unit(int u, const Params& prm) {
+  KvUnit x;
+  int64_t uu = u;
+  x.kb = (int)(uu % prm.nb); uu /= prm.nb;
+  x.hk = (int)(uu % prm.Hkv); uu /= prm.Hkv;
+  x.b = (int)(uu % prm.B);
+  const int idx = (int)(uu / prm.B);
+  x.NBQ = 0;
+  x.ok = idx >= 0 && idx < prm.n_kv_items;
+  if (!x.ok) return x;
+  x.it = prm.kv_items[idx];
+  x.ok = x.it.p >= 0 && x.it.p < prm.P && x.it.slot >= 0 && x.it.slot < prm.n_kv_slots && x.it.n_kv >= 1 &&
+         x.it.kv_off >= 0;
+  // query blocks of the unit: heads of the group x Q partitions of the slot x blocks
+  if (x.ok)
+    for (int qi = 0; qi < x.it.n_kv; ++qi)
+      x.NBQ += prm.nb - qblock_begin(x.it.p, __ldg(prm.q_list + x.it.kv_off + qi), prm.causal, x.kb);
+  x.NBQ *= prm.Hq / prm.Hkv;
+  return x;
+}
+// A unit travels through the shared-memory ring decoded (16 ints per entry), so that consumers
+// never wait on the global reads of the decode.
+__device__ __forceinline__ void put_unit(volatile int32_t* e, int u, const KvUnit& x) {
+  e[0] = u;
+  e[1] = x.kb, e[2] = x.hk, e[3] = x.b, e[4] = x.NBQ, e[5] = x.ok ? 1 : 0;
+  e[6] = x.it.p, e[7] = x.it.slot, e[8] = x.it.kv_off, e[9] = x.it.n_kv;
+}
+__device__ __forceinline__ int get_unit(const volatile int32_t* e, KvUnit& x) {
+  x.kb = e[1], x.hk = e[2], x.b = e[3], x.NBQ = e[4], x.ok = e[5] != 0;
+  x.it.p = e[6], x.it.slot = e[7], x.it.kv_off = e[8], x.it.n_kv = e[9];
+  return e[0];
+}
+
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -225,32 +270,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto bar = [&](int i) { return sb + Ly::BAR_OFF + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::MISC_OFF);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + Ly::MISC_OFF + 4);
+  volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(smem + Ly::RING_OFF);
   float* nlse_s = reinterpret_cast<float*>(smem + Ly::VEC_OFF);  // [2][BM] -LSE log2 e of the query columns
   float* ndsum_s = nlse_s + 2 * BM;                              // [2][BM] -D
   const int64_t L = prm.L;
-
-  // unit -> (KV slot, batch, KV head, key block)
-  int64_t uu = blockIdx.x;
-  const int kb = (int)(uu % prm.nb); uu /= prm.nb;
-  const int hk = (int)(uu % prm.Hkv); uu /= prm.Hkv;
-  const int b = (int)(uu % prm.B);
-  const int idx = (int)(uu / prm.B);
-  const DevItem it = prm.kv_items[idx];  // {k, kv slot, q_off, n_q}
-  const bool unit_ok = it.p >= 0 && it.p < prm.P && it.slot >= 0 && it.slot < prm.n_kv_slots && it.n_kv >= 1 &&
-                       it.kv_off >= 0;
-  const int k = it.p;
   const int g = prm.Hq / prm.Hkv;
-  // query blocks of the unit: heads of the group x Q partitions of the slot x blocks
-  int NBQ = 0;
-  if (unit_ok)
-    for (int qi = 0; qi < it.n_kv; ++qi) {
-      const int p = __ldg(prm.q_list + it.kv_off + qi);
-      NBQ += prm.nb - qblock_begin(k, p, prm.causal, kb);
-    }
-  NBQ *= g;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Ly::B_RES), 1);
+    mbar_init(bar(Ly::B_RESE), 1);
     for (int s = 0; s < Ly::NSA; ++s) {
       mbar_init(bar(Ly::B_AF + s), 1);
       mbar_init(bar(Ly::B_AE + s), 1);
@@ -260,16 +288,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(Ly::B_BE + s), 1);
     }
     mbar_init(bar(Ly::B_S), 1);
-    mbar_init(bar(Ly::B_S + 1), 1);
     mbar_init(bar(Ly::B_DP), 1);
     mbar_init(bar(Ly::B_P), N_EW);  // one lane of each elementwise warp
     mbar_init(bar(Ly::B_DS), N_EW);
     mbar_init(bar(Ly::B_ACC), 1);
+    mbar_init(bar(Ly::B_ACCE), N_EW);
     mbar_init(bar(Ly::B_DRAIN), 1);
     mbar_init(bar(Ly::B_VEC), BM);  // every elementwise thread has written its LSE / D value
     mbar_init(bar(Ly::B_VEC + 1), BM);
-    *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0 || !unit_ok) ? 1 : 0;
-    if (!unit_ok) record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_ITEM, (int32_t)blockIdx.x);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(Ly::B_UF + s), 1);
+      mbar_init(bar(Ly::B_UE + s), N_EW + 1);  // the elementwise warps and the MMA warp read a unit
+    }
+    *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0) ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -289,22 +320,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const bool run = *abort_flag == 0;
 
-  // the i-th query block of the unit: head, partition, block
-  auto block_at = [&](int i, int& h, int& p, int& qb) {
-    const int per_head = NBQ / g;
-    h = hk * g + i / per_head;
-    int r = i % per_head;
-    for (int qi = 0; qi < it.n_kv; ++qi) {
-      p = __ldg(prm.q_list + it.kv_off + qi);
-      const int b0 = qblock_begin(k, p, prm.causal, kb);
-      if (r < prm.nb - b0) {
-        qb = b0 + r;
-        return;
-      }
-      r -= prm.nb - b0;
+  int nu = 0;
+  auto take = [&](int& v, KvUnit& y, int role) -> bool {
+    const int slot = nu & 1;
+    bool r = mbar_wait_warp(bar(Ly::B_UF + slot), (uint32_t)((nu >> 1) & 1), prm.wait_limit_ns, abort_flag,
+                            prm.status, role, -1);
+    if (!r) return false;
+    v = get_unit(unit_ring + 16 * slot, y);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(Ly::B_UE + slot));
+    ++nu;
+    return true;
+  };
+  auto bad_unit = [&](int u, int role) {
+    if (lane == 0) {
+      record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, role, u);
+      *abort_flag = 1;
     }
-    p = -1;
-    qb = 0;
+    __syncwarp();
   };
 
   if (warp < N_EW) {
@@ -318,128 +351,172 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tm_dv = tmem + lane_base + 256u;
     const uint32_t tm_dk = tmem + lane_base + 256u + (uint32_t)D;
     bool ok = run;
-    // Query-block cursors: `cur` is block i, `nxt` block i + 1.  Stepping them keeps the global
-    // reads of the slot's partition list off the per-block path (one read per partition change).
-    QCursor cur, nxt;
-    cur.start(prm, it, k, kb, hk * g);
-    nxt = cur;
     // LSE and D of query column `row` for the next block, loaded raw one block ahead by the first
     // column half and only used (scaled, published) at the top of the next iteration, so that the
-    // loads never stall the block in flight
+    // loads never stall the block in flight; across units, the next unit's first block is
+    // loaded before this unit's epilogue
     float raw_lse = 0.f, raw_d = 0.f;
     bool raw_in = false;
-    auto fetch = [&](const QCursor& c) {
+    auto fetch = [&](const KvUnit& y, const QCursor& c) {
       const int64_t ql = (int64_t)c.qb * BM + row;
       raw_in = c.p >= 0 && c.p < prm.P && ql < L;
       if (raw_in) {
-        const int64_t gi = ((int64_t)b * prm.Hq + c.h) * prm.S + (int64_t)c.p * L + ql;
+        const int64_t gi = ((int64_t)y.b * prm.Hq + c.h) * prm.S + (int64_t)c.p * L + ql;
         raw_lse = __ldg(prm.lse + gi);
         raw_d = __ldg(prm.dsum + gi);
       }
     };
-    if (ok && NBQ > 0 && hf == 0) fetch(cur);
-    for (int i = 0; i < NBQ && ok; ++i) {
-      const int vb = i & 1;
-      if (i > 0) cur = nxt;
-      if (i + 1 < NBQ) nxt.step(prm, it, k, kb);
-      // publish this column's values, then wait (bounded) until all 128 columns are written; a
-      // buffer is rewritten two blocks later, after every writer has arrived for the block between
-      if (hf == 0) {
-        // no such query row: exp2(s - inf) = 0, so it needs no mask
-        nlse_s[vb * BM + row] = raw_in ? -raw_lse * LOG2E : -INFINITY;
-        ndsum_s[vb * BM + row] = raw_in ? -raw_d : 0.f;
-        mbar_arrive(bar(Ly::B_VEC + vb));
-        if (i + 1 < NBQ) fetch(nxt);
+    int v = -1;
+    KvUnit x;
+    if (ok) ok = take(v, x, ROLE_EW);
+    // Query-block cursors: `cur` is block i, `nxt` block i + 1.  Stepping them keeps the global
+    // reads of the slot's partition list off the per-block path (one read per partition change).
+    QCursor cur, nxt;
+    if (ok && v >= 0) {
+      if (x.ok) {
+        cur.start(prm, x.it, x.it.p, x.kb, x.hk * g);
+        if (hf == 0) fetch(x, cur);
       }
-      ok = mbar_wait(bar(Ly::B_VEC + vb), (uint32_t)((i >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
-                     ROLE_EW, i);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      const int p = cur.p, qb = cur.qb;
-      // causal diagonal block: query columns before this key row are masked (query rows past the
-      // partition end carry -inf in place of -LSE and need no mask)
-      const int lo = (prm.causal && p == k && qb == kb) ? row - c_base : 0;
-      ok = mbar_wait(bar(Ly::B_S), (uint32_t)(i & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, i);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      float pv[64];
-      tmem_ld32(tm_s + (uint32_t)c_base, pv);
-      tmem_ld32(tm_s + (uint32_t)c_base + 32u, pv + 32);
-      tc_wait_ld();
-      if (__any_sync(0xffffffffu, lo > 0)) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c < lo) pv[c] = -INFINITY;
+    }
+    int64_t g0 = 0;  // global index of the unit's first query block
+    int k_unit = 0;
+    while (ok && v >= 0) {
+      if (!x.ok || x.NBQ < 1) {
+        bad_unit(v, ROLE_EW);
+        ok = false;
+        break;
       }
-      const float4* lv = reinterpret_cast<const float4*>(nlse_s + vb * BM + c_base);
-      const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2);
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 64; c += 4) {
-        const float4 l4 = lv[c / 4];
-        float x0, x1, x2, x3;
-        f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), sc2, f2_pack(l4.x, l4.y)), x0, x1);
-        f2_unpack(f2_fma(f2_pack(pv[c + 2], pv[c + 3]), sc2, f2_pack(l4.z, l4.w)), x2, x3);
-        pv[c] = fast_exp2(x0);
-        pv[c + 1] = fast_exp2(x1);
-        pv[c + 2] = fast_exp2(x2);
-        pv[c + 3] = fast_exp2(x3);
-        pk[c / 2] = pack_bf16x2(pv[c], pv[c + 1]);
-        pk[c / 2 + 1] = pack_bf16x2(pv[c + 2], pv[c + 3]);
-      }
-      tmem_st32(tm_s + (uint32_t)c_base, pk);  // P^T columns of this half (see packed_col)
-      tc_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(Ly::B_P));
-      ok = mbar_wait(bar(Ly::B_DP), (uint32_t)(i & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, i);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      {
-        float dp[64];
-        tmem_ld32(tm_dp + (uint32_t)c_base, dp);
-        tmem_ld32(tm_dp + (uint32_t)c_base + 32u, dp + 32);
+      const int k = x.it.p, kb = x.kb, NBQ = x.NBQ;
+      nxt = cur;
+      for (int i = 0; i < NBQ && ok; ++i) {
+        const int64_t gi = g0 + i;
+        const int vb = (int)(gi & 1);
+        if (i > 0) cur = nxt;
+        if (i + 1 < NBQ) nxt.step(prm, x.it, k, kb);
+        // publish this column's values, then wait (bounded) until all 128 columns are written; a
+        // buffer is rewritten two blocks later, after every writer has arrived for the block between
+        if (hf == 0) {
+          // no such query row: exp2(s - inf) = 0, so it needs no mask
+          nlse_s[vb * BM + row] = raw_in ? -raw_lse * LOG2E : -INFINITY;
+          ndsum_s[vb * BM + row] = raw_in ? -raw_d : 0.f;
+          mbar_arrive(bar(Ly::B_VEC + vb));
+          if (i + 1 < NBQ) fetch(x, nxt);
+        }
+        ok = mbar_wait(bar(Ly::B_VEC + vb), (uint32_t)((gi >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                       ROLE_EW, i);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const int p = cur.p, qb = cur.qb;
+        // causal diagonal block: query columns before this key row are masked (query rows past the
+        // partition end carry -inf in place of -LSE and need no mask)
+        const int lo = (prm.causal && p == k && qb == kb) ? row - c_base : 0;
+        ok = mbar_wait(bar(Ly::B_S), (uint32_t)(gi & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, i);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        float pv[64];
+        tmem_ld32(tm_s + (uint32_t)c_base, pv);
+        tmem_ld32(tm_s + (uint32_t)c_base + 32u, pv + 32);
         tc_wait_ld();
-        const float4* dv_ = reinterpret_cast<const float4*>(ndsum_s + vb * BM + c_base);
-        uint32_t ds2[32];
+        if (__any_sync(0xffffffffu, lo > 0)) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < lo) pv[c] = -INFINITY;
+        }
+        const float4* lv = reinterpret_cast<const float4*>(nlse_s + vb * BM + c_base);
+        const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2);
+        uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
-          const float4 d4 = dv_[c / 4];
-          float a0, a1, a2, a3;
-          f2_unpack(f2_mul(f2_add(f2_pack(dp[c], dp[c + 1]), f2_pack(d4.x, d4.y)), f2_pack(pv[c], pv[c + 1])), a0, a1);
-          f2_unpack(f2_mul(f2_add(f2_pack(dp[c + 2], dp[c + 3]), f2_pack(d4.z, d4.w)), f2_pack(pv[c + 2], pv[c + 3])),
-                    a2, a3);
-          ds2[c / 2] = pack_bf16x2(a0, a1);
-          ds2[c / 2 + 1] = pack_bf16x2(a2, a3);
+          const float4 l4 = lv[c / 4];
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), sc2, f2_pack(l4.x, l4.y)), x0, x1);
+          f2_unpack(f2_fma(f2_pack(pv[c + 2], pv[c + 3]), sc2, f2_pack(l4.z, l4.w)), x2, x3);
+          pv[c] = fast_exp2(x0);
+          pv[c + 1] = fast_exp2(x1);
+          pv[c + 2] = fast_exp2(x2);
+          pv[c + 3] = fast_exp2(x3);
+          pk[c / 2] = pack_bf16x2(pv[c], pv[c + 1]);
+          pk[c / 2 + 1] = pack_bf16x2(pv[c + 2], pv[c + 3]);
         }
-        tmem_st32(tm_dp + (uint32_t)c_base, ds2);  // dS^T columns of this half
+        tmem_st32(tm_s + (uint32_t)c_base, pk);  // P^T columns of this half (see packed_col)
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(Ly::B_P));
+        ok = mbar_wait(bar(Ly::B_DP), (uint32_t)(gi & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, i);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        {
+          float dp[64];
+          tmem_ld32(tm_dp + (uint32_t)c_base, dp);
+          tmem_ld32(tm_dp + (uint32_t)c_base + 32u, dp + 32);
+          tc_wait_ld();
+          const float4* dv_ = reinterpret_cast<const float4*>(ndsum_s + vb * BM + c_base);
+          uint32_t ds2[32];
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            const float4 d4 = dv_[c / 4];
+            float a0, a1, a2, a3;
+            f2_unpack(f2_mul(f2_add(f2_pack(dp[c], dp[c + 1]), f2_pack(d4.x, d4.y)), f2_pack(pv[c], pv[c + 1])), a0,
+                      a1);
+            f2_unpack(f2_mul(f2_add(f2_pack(dp[c + 2], dp[c + 3]), f2_pack(d4.z, d4.w)), f2_pack(pv[c + 2], pv[c + 3])),
+                      a2, a3);
+            ds2[c / 2] = pack_bf16x2(a0, a1);
+            ds2[c / 2 + 1] = pack_bf16x2(a2, a3);
+          }
+          tmem_st32(tm_dp + (uint32_t)c_base, ds2);  // dS^T columns of this half
+        }
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(Ly::B_DS));
       }
-      tc_wait_st();
+      if (!ok) break;
+      // the next unit, and its first block's LSE and D, before this unit's epilogue
+      int vn = -1;
+      KvUnit xn;
+      ok = take(vn, xn, ROLE_EW);
+      if (!ok) break;
+      if (vn >= 0) {
+        if (xn.ok) {
+          cur.start(prm, xn.it, xn.it.p, xn.kb, xn.hk * g);
+          if (hf == 0) fetch(xn, cur);
+        }
+      }
+      // ---- epilogue: this half's columns of the dV and dK rows of this key block
+      ok = mbar_wait(bar(Ly::B_ACC), (uint32_t)(k_unit & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, -1);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int64_t row0 =
+          (((int64_t)x.b * prm.Hkv + x.hk) * prm.n_kv_slots + x.it.slot) * L + (int64_t)kb * BM + wq * 32;
+      const int rows_valid = (int)max((int64_t)0, min((int64_t)32, L - ((int64_t)kb * BM + wq * 32)));
+      // copy both accumulators' columns out of TMEM in two halves (registers), releasing TMEM
+      // after the second, then store
+      float acc[D / 2];
+#pragma unroll
+      for (int c = 0; c < D / 2; c += 32) tmem_ld32(tm_dv + (uint32_t)(hf * (D / 2) + c), acc + c);
+      tc_wait_ld();
+#pragma unroll
+      for (int c = 0; c < D / 2; c += 32)
+        store_rows<D>(*reinterpret_cast<const float(*)[32]>(acc + c), 1.f, prm.dv_part, row0, rows_valid,
+                      hf * (D / 2) + c, lane);
+#pragma unroll
+      for (int c = 0; c < D / 2; c += 32) tmem_ld32(tm_dk + (uint32_t)(hf * (D / 2) + c), acc + c);
+      tc_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(Ly::B_DS));
-    }
-    // ---- epilogue: this half's columns of the dV and dK rows of this key block
-    if (ok) {
-      ok = mbar_wait(bar(Ly::B_ACC), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, -1);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      tc_fence_after();
-      const int64_t row0 = (((int64_t)b * prm.Hkv + hk) * prm.n_kv_slots + it.slot) * L + (int64_t)kb * BM + wq * 32;
-      const int rows_valid = (int)max((int64_t)0, min((int64_t)32, L - ((int64_t)kb * BM + wq * 32)));
-#pragma unroll 1
-      for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
-        float v[32];
-        tmem_ld32(tm_dv + (uint32_t)c, v);
-        tc_wait_ld();
-        store_rows<D>(v, 1.f, prm.dv_part, row0, rows_valid, c, lane);
-        tmem_ld32(tm_dk + (uint32_t)c, v);
-        tc_wait_ld();
-        store_rows<D>(v, prm.scale, prm.dk_part, row0, rows_valid, c, lane);
-      }
+      if (lane == 0) mbar_arrive(bar(Ly::B_ACCE));
+#pragma unroll
+      for (int c = 0; c < D / 2; c += 32)
+        store_rows<D>(*reinterpret_cast<const float(*)[32]>(acc + c), prm.scale, prm.dk_part, row0, rows_valid,
+                      hf * (D / 2) + c, lane);
+      g0 += NBQ;
+      ++k_unit;
+      v = vn;
+      x = xn;
     }
   } else if (warp == WARP_MMA) {
     // ================================================================ MMA issuer
@@ -452,126 +529,220 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint64_t a_mn = smem_desc_sw128(sb + Ly::A0, Ly::BOX, 1024u);
     const uint64_t b_kmaj = smem_desc_sw128(sb + Ly::B0, 16u, 1024u);   // dO stages
     const uint64_t b_mn = smem_desc_sw128(sb + Ly::B0, Ly::BOX, 1024u);
-    auto issue_s = [&](int sa) {  // S^T = K Q^T
-      const uint64_t qd = a_kmaj + (uint64_t)sa * TILE16;
+    auto issue_s = [&](int64_t gi) {  // S^T = K Q(gi)^T
+      const uint64_t qd = a_kmaj + (uint64_t)(gi % Ly::NSA) * TILE16;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         tc_mma_ss_warp(tmem, kdesc + kmaj_off<D>(kk), qd + kmaj_off<D>(kk), idesc_ss, kk > 0);
       tc_commit_warp(bar(Ly::B_S));
     };
-    auto issue_dp = [&](int sbb) {  // dP^T = V dO^T
-      const uint64_t gd = b_kmaj + (uint64_t)sbb * TILE16;
+    auto issue_dp = [&](int64_t gi) {  // dP^T = V dO(gi)^T
+      const uint64_t gd = b_kmaj + (uint64_t)(gi % Ly::NSB) * TILE16;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         tc_mma_ss_warp(tmem + 128u, vdesc + kmaj_off<D>(kk), gd + kmaj_off<D>(kk), idesc_ss, kk > 0);
       tc_commit_warp(bar(Ly::B_DP));
     };
-    auto issue_dv = [&](int sbb, bool first) {  // dV += P^T dO
+    auto issue_dv = [&](int64_t gi, bool first) {  // dV += P^T dO(gi)
+      const int sbb = (int)(gi % Ly::NSB);
       const uint64_t gd = b_mn + (uint64_t)sbb * TILE16;
 #pragma unroll
       for (int kk = 0; kk < BM / 16; ++kk)
         tc_mma_ts_warp(tmem + 256u, tmem + packed_col(kk), gd + (uint64_t)(kk * 128), idesc_ts,
                        (!first || kk > 0) ? 1u : 0u);
+      tc_commit_warp(bar(Ly::B_BE + sbb));  // dO(gi): read by dP^T(gi) and dV(gi)
     };
-    auto issue_dk = [&](int sa, bool first) {  // dK += dS^T Q
+    auto issue_dk = [&](int64_t gi, bool first) {  // dK += dS^T Q(gi)
+      const int sa = (int)(gi % Ly::NSA);
       const uint64_t qd = a_mn + (uint64_t)sa * TILE16;
 #pragma unroll
       for (int kk = 0; kk < BM / 16; ++kk)
         tc_mma_ts_warp(tmem + 256u + (uint32_t)D, tmem + 128u + packed_col(kk), qd + (uint64_t)(kk * 128),
                        idesc_ts, (!first || kk > 0) ? 1u : 0u);
+      tc_commit_warp(bar(Ly::B_AE + sa));  // Q(gi): read by S^T(gi) and dK(gi)
     };
-    auto wait_a = [&](int i) {  // Q(i) landed
-      return mbar_wait_warp(bar(Ly::B_AF + i % Ly::NSA), (uint32_t)((i / Ly::NSA) & 1), prm.wait_limit_ns, abort_flag,
-                            prm.status, ROLE_MMA, i);
+    auto wait_a = [&](int64_t gi) {  // Q(gi) landed
+      return mbar_wait_warp(bar(Ly::B_AF + (int)(gi % Ly::NSA)), (uint32_t)((gi / Ly::NSA) & 1), prm.wait_limit_ns,
+                            abort_flag, prm.status, ROLE_MMA, (int32_t)gi);
     };
-    auto wait_b = [&](int i) {  // dO(i) landed
-      return mbar_wait_warp(bar(Ly::B_BF + i % Ly::NSB), (uint32_t)((i / Ly::NSB) & 1), prm.wait_limit_ns, abort_flag,
-                            prm.status, ROLE_MMA, i);
+    auto wait_b = [&](int64_t gi) {  // dO(gi) landed
+      return mbar_wait_warp(bar(Ly::B_BF + (int)(gi % Ly::NSB)), (uint32_t)((gi / Ly::NSB) & 1), prm.wait_limit_ns,
+                            abort_flag, prm.status, ROLE_MMA, (int32_t)gi);
     };
-    bool ok = run && NBQ > 0;
-    if (ok) ok = mbar_wait_warp(bar(Ly::B_RES), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, -1);
-    if (ok) ok = wait_a(0) && wait_b(0);
-    if (ok) {
+    int nres = 0;
+    // S^T(0) and dP^T(0) of a unit whose first block is gi, as soon as its resident K and V have
+    // landed (for every unit but the first, after the previous unit's last dK)
+    auto start_unit = [&](const KvUnit& y, int64_t gi) -> bool {
+      if (!mbar_wait_warp(bar(Ly::B_RES), (uint32_t)(nres & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                          ROLE_MMA, -1))
+        return false;
+      ++nres;
+      if (!wait_a(gi)) return false;
       tc_fence_after();
-      issue_s(0);
-      issue_dp(0);
-    }
-    for (int i = 0; i < NBQ && ok; ++i) {
-      ok = mbar_wait_warp(bar(Ly::B_P), (uint32_t)(i & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, i);
-      if (!ok) break;
+      issue_s(gi);
+      if (!wait_b(gi)) return false;
       tc_fence_after();
-      issue_dv(i % Ly::NSB, i == 0);
-      tc_commit_warp(bar(Ly::B_BE + i % Ly::NSB));  // dO(i): read by dP^T(i) and dV(i)
-      if (i + 1 < NBQ) {
-        ok = wait_a(i + 1);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s((i + 1) % Ly::NSA);
-      }
-      ok = mbar_wait_warp(bar(Ly::B_DS), (uint32_t)(i & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, i);
-      if (!ok) break;
-      tc_fence_after();
-      issue_dk(i % Ly::NSA, i == 0);
-      tc_commit_warp(bar(Ly::B_AE + i % Ly::NSA));  // Q(i): read by S^T(i) and dK(i)
-      if (i + 1 < NBQ) {
-        ok = wait_b(i + 1);
-        if (!ok) break;
-        tc_fence_after();
-        issue_dp((i + 1) % Ly::NSB);
+      issue_dp(gi);
+      if (y.NBQ == 1) tc_commit_warp(bar(Ly::B_RESE));  // the unit's last S^T and dP^T are issued
+      return true;
+    };
+    bool ok = run;
+    int v = -1;
+    KvUnit x;
+    if (ok) ok = take(v, x, ROLE_MMA);
+    if (ok && v >= 0) {
+      if (!x.ok || x.NBQ < 1) {
+        bad_unit(v, ROLE_MMA);
+        ok = false;
+      } else {
+        ok = start_unit(x, 0);
       }
     }
-    if (ok) tc_commit_warp(bar(Ly::B_ACC));
+    int64_t g0 = 0;
+    int k_unit = 0;
+    while (ok && v >= 0) {
+      const int NBQ = x.NBQ;
+      for (int i = 0; i < NBQ && ok; ++i) {
+        const int64_t gi = g0 + i;
+        ok = mbar_wait_warp(bar(Ly::B_P), (uint32_t)(gi & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, i);
+        if (!ok) break;
+        if (i == 0 && k_unit > 0) {  // the previous unit's dV and dK have been copied out of TMEM
+          ok = mbar_wait_warp(bar(Ly::B_ACCE), (uint32_t)((k_unit - 1) & 1), prm.wait_limit_ns, abort_flag,
+                              prm.status, ROLE_MMA, -1);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        issue_dv(gi, i == 0);
+        if (i + 1 < NBQ) {
+          ok = wait_a(gi + 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(gi + 1);
+        }
+        ok = mbar_wait_warp(bar(Ly::B_DS), (uint32_t)(gi & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, i);
+        if (!ok) break;
+        tc_fence_after();
+        issue_dk(gi, i == 0);
+        if (i + 1 == NBQ) tc_commit_warp(bar(Ly::B_ACC));
+        if (i + 1 < NBQ) {
+          ok = wait_b(gi + 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(gi + 1);
+          if (i + 2 == NBQ) tc_commit_warp(bar(Ly::B_RESE));  // the unit's last S^T and dP^T are issued
+        }
+      }
+      if (!ok) break;
+      int vn = -1;
+      ok = take(vn, x, ROLE_MMA);
+      if (!ok) break;
+      g0 += NBQ;
+      ++k_unit;
+      v = vn;
+      if (v < 0) break;
+      if (!x.ok || x.NBQ < 1) {
+        bad_unit(v, ROLE_MMA);
+        ok = false;
+        break;
+      }
+      ok = start_unit(x, g0);
+    }
+    // exit-path drain: every MMA issued completes before TMEM is freed
     tc_commit_warp(bar(Ly::B_DRAIN));
     mbar_drain(bar(Ly::B_DRAIN), 0u, DRAIN_NS);
   } else if (warp == WARP_LOAD && lane == 0) {
     // ================================================================ producer
-    bool ok = run && NBQ > 0;
-    const int64_t kvrow = ((int64_t)b * prm.Hkv + hk) * prm.S + (int64_t)k * L + (int64_t)kb * BM;
-    if (ok) {
+    bool ok = run;
+    int np = 0;  // units published
+    auto publish = [&](KvUnit& y) -> int {
+      const int slot = np & 1;
+      ok = mbar_wait(bar(Ly::B_UE + slot), (uint32_t)(((np >> 1) & 1) ^ 1), prm.wait_limit_ns, abort_flag,
+                     prm.status, ROLE_LOAD, -1);
+      if (!ok) return -1;
+      int u = (int)atomicAdd(prm.counter_kv, 1u);
+      if (u >= prm.n_kv_units) u = -1;
+      if (u >= 0) y = kv_unit(u, prm);
+      put_unit(unit_ring + 16 * slot, u, y);
+      mbar_arrive(bar(Ly::B_UF + slot));
+      ++np;
+      return u;
+    };
+    int nres = 0;
+    int64_t ga = 0, gb = 0;  // Q and dO blocks issued
+    KvUnit x, y;
+    int u = ok ? publish(x) : -1;
+    while (ok && u >= 0) {
+      if (!x.ok || x.NBQ < 1) {
+        record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_LOAD, u);
+        *abort_flag = 1;
+        break;
+      }
+      // publish the following unit now and pull its K, V rows into L2
+      const int un = publish(y);
+      if (!ok) break;
+      if (un >= 0) {
+        if (y.ok) {
+          const int64_t kn = ((int64_t)y.b * prm.Hkv + y.hk) * prm.S + (int64_t)y.it.p * L + (int64_t)y.kb * BM;
+          for (int c = 0; c < D / 64; ++c) {
+            tma_prefetch_l2_2d(&tmK, c * 64, (int32_t)kn);
+            tma_prefetch_l2_2d(&tmV, c * 64, (int32_t)kn);
+          }
+        }
+      }
+      // resident K and V: the previous unit's last S^T and dP^T products must be done with them
+      ok = mbar_wait(bar(Ly::B_RESE), (uint32_t)((nres & 1) ^ 1), prm.wait_limit_ns, abort_flag, prm.status,
+                     ROLE_LOAD, u);
+      if (!ok) break;
+      const int64_t kvrow = ((int64_t)x.b * prm.Hkv + x.hk) * prm.S + (int64_t)x.it.p * L + (int64_t)x.kb * BM;
       mbar_expect_tx(bar(Ly::B_RES), 2 * Ly::TILE);
       for (int c = 0; c < D / 64; ++c) {
         tma_load_2d(sb + Ly::RES0 + (uint32_t)c * Ly::BOX, &tmK, c * 64, (int32_t)kvrow, bar(Ly::B_RES));
         tma_load_2d(sb + Ly::RES1 + (uint32_t)c * Ly::BOX, &tmV, c * 64, (int32_t)kvrow, bar(Ly::B_RES));
       }
-    }
-    int issued_a = 0, issued_b = 0;
-    for (int i = 0; i < NBQ && ok; ++i) {
-      int h, p, qb;
-      block_at(i, h, p, qb);
-      if (p < 0 || p >= prm.P) {
-        record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_LOAD, (int32_t)blockIdx.x);
-        *abort_flag = 1;
-        break;
+      ++nres;
+      QCursor cur;
+      cur.start(prm, x.it, x.it.p, x.kb, x.hk * g);
+      for (int i = 0; i < x.NBQ && ok; ++i) {
+        if (i > 0) cur.step(prm, x.it, x.it.p, x.kb);
+        if (cur.p < 0 || cur.p >= prm.P) {
+          record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_LOAD, u);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        const int32_t qrow =
+            (int32_t)(((int64_t)x.b * prm.Hq + cur.h) * prm.S + (int64_t)cur.p * L + (int64_t)cur.qb * BM);
+        const int sa = (int)(ga % Ly::NSA), sbb = (int)(gb % Ly::NSB);
+        if (ga >= Ly::NSA) {
+          ok = mbar_wait(bar(Ly::B_AE + sa), (uint32_t)((ga / Ly::NSA - 1) & 1), prm.wait_limit_ns, abort_flag,
+                         prm.status, ROLE_LOAD, i);
+          if (!ok) break;
+        }
+        mbar_expect_tx(bar(Ly::B_AF + sa), Ly::TILE);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(sb + Ly::A0 + (uint32_t)sa * Ly::TILE + (uint32_t)c * Ly::BOX, &tmQ, c * 64, qrow,
+                      bar(Ly::B_AF + sa));
+        ++ga;
+        if (gb >= Ly::NSB) {
+          ok = mbar_wait(bar(Ly::B_BE + sbb), (uint32_t)((gb / Ly::NSB - 1) & 1), prm.wait_limit_ns, abort_flag,
+                         prm.status, ROLE_LOAD, i);
+          if (!ok) break;
+        }
+        mbar_expect_tx(bar(Ly::B_BF + sbb), Ly::TILE);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(sb + Ly::B0 + (uint32_t)sbb * Ly::TILE + (uint32_t)c * Ly::BOX, &tmG, c * 64, qrow,
+                      bar(Ly::B_BF + sbb));
+        ++gb;
       }
-      const int32_t qrow = (int32_t)(((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + (int64_t)qb * BM);
-      const int sa = i % Ly::NSA, sbb = i % Ly::NSB;
-      if (i >= Ly::NSA) {
-        ok = mbar_wait(bar(Ly::B_AE + sa), (uint32_t)((i / Ly::NSA - 1) & 1), prm.wait_limit_ns, abort_flag,
-                       prm.status, ROLE_LOAD, i);
-        if (!ok) break;
-      }
-      mbar_expect_tx(bar(Ly::B_AF + sa), Ly::TILE);
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_2d(sb + Ly::A0 + (uint32_t)sa * Ly::TILE + (uint32_t)c * Ly::BOX, &tmQ, c * 64, qrow,
-                    bar(Ly::B_AF + sa));
-      ++issued_a;
-      if (i >= Ly::NSB) {
-        ok = mbar_wait(bar(Ly::B_BE + sbb), (uint32_t)((i / Ly::NSB - 1) & 1), prm.wait_limit_ns, abort_flag,
-                       prm.status, ROLE_LOAD, i);
-        if (!ok) break;
-      }
-      mbar_expect_tx(bar(Ly::B_BF + sbb), Ly::TILE);
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_2d(sb + Ly::B0 + (uint32_t)sbb * Ly::TILE + (uint32_t)c * Ly::BOX, &tmG, c * 64, qrow,
-                    bar(Ly::B_BF + sbb));
-      ++issued_b;
+      u = un;
+      x = y;
     }
     // exit-path drain: every load issued lands before the CTA exits
-    if (run && NBQ > 0) mbar_drain(bar(Ly::B_RES), 0u, DRAIN_NS);
-    for (int j = (issued_a > Ly::NSA ? issued_a - Ly::NSA : 0); j < issued_a; ++j)
-      mbar_drain(bar(Ly::B_AF + j % Ly::NSA), (uint32_t)((j / Ly::NSA) & 1), DRAIN_NS);
-    for (int j = (issued_b > Ly::NSB ? issued_b - Ly::NSB : 0); j < issued_b; ++j)
-      mbar_drain(bar(Ly::B_BF + j % Ly::NSB), (uint32_t)((j / Ly::NSB) & 1), DRAIN_NS);
+    if (nres > 0) mbar_drain(bar(Ly::B_RES), (uint32_t)((nres - 1) & 1), DRAIN_NS);
+    for (int64_t j = (ga > Ly::NSA ? ga - Ly::NSA : 0); j < ga; ++j)
+      mbar_drain(bar(Ly::B_AF + (int)(j % Ly::NSA)), (uint32_t)((j / Ly::NSA) & 1), DRAIN_NS);
+    for (int64_t j = (gb > Ly::NSB ? gb - Ly::NSB : 0); j < gb; ++j)
+      mbar_drain(bar(Ly::B_BF + (int)(j % Ly::NSB)), (uint32_t)((j / Ly::NSB) & 1), DRAIN_NS);
   }
 
   tc_fence_before();
@@ -583,6 +754,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ================================================================== dQ
+// unit -> (work item, batch, head, 128-row query block), query block fastest
+struct DqUnit {
+  int qb, h, b, hk, NB;
+  DevItem it;
+  bool ok;
+};
+__device__ __forceinline__ DqUnit dq_unit(int u, const Params& prm) {
+  DqUnit x;
+  int64_t uu = u;
+  x.qb = (int)(uu % prm.nb); uu /= prm.nb;
+  x.h = (int)(uu % prm.Hq); uu /= prm.Hq;
+  x.b = (int)(uu % prm.B);
+  const int idx = (int)(uu / prm.B);
+  x.hk = x.h / (prm.Hq / prm.Hkv);
+  x.NB = 0;
+  x.ok = idx >= 0 && idx < prm.n_items;
+  if (!x.ok) return x;
+  x.it = prm.items[idx];  // {p, slot, kv_off, n_kv}
+  x.ok = x.it.p >= 0 && x.it.p < prm.P && x.it.slot >= 0 && x.it.slot < prm.n_slots && x.it.n_kv >= 1 &&
+         x.it.kv_off >= 0;
+  if (x.ok)
+    for (int ki = 0; ki < x.it.n_kv; ++ki)
+      x.NB += kblocks_of(__ldg(prm.kv_list + x.it.kv_off + ki), x.it.p, prm.causal, prm.nb, x.qb);
+  return x;
+}
+__device__ __forceinline__ void put_unit(volatile int32_t* e, int u, const DqUnit& x) {
+  e[0] = u;
+  e[1] = x.qb, e[2] = x.h, e[3] = x.b, e[4] = x.NB, e[5] = x.ok ? 1 : 0, e[10] = x.hk;
+  e[6] = x.it.p, e[7] = x.it.slot, e[8] = x.it.kv_off, e[9] = x.it.n_kv;
+}
+__device__ __forceinline__ int get_unit(const volatile int32_t* e, DqUnit& x) {
+  x.qb = e[1], x.h = e[2], x.b = e[3], x.NB = e[4], x.ok = e[5] != 0, x.hk = e[10];
+  x.it.p = e[6], x.it.slot = e[7], x.it.kv_off = e[8], x.it.n_kv = e[9];
+  return e[0];
+}
+
 template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -600,25 +807,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto bar = [&](int i) { return sb + Ly::BAR_OFF + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::MISC_OFF);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + Ly::MISC_OFF + 4);
+  volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(smem + Ly::RING_OFF);
   const int64_t L = prm.L;
-
-  // unit -> (work item, batch, head, query block)
-  int64_t uu = blockIdx.x;
-  const int qb = (int)(uu % prm.nb); uu /= prm.nb;
-  const int h = (int)(uu % prm.Hq); uu /= prm.Hq;
-  const int b = (int)(uu % prm.B);
-  const int idx = (int)(uu / prm.B);
-  const DevItem it = prm.items[idx];  // {p, slot, kv_off, n_kv}
-  const bool unit_ok = it.p >= 0 && it.p < prm.P && it.slot >= 0 && it.slot < prm.n_slots && it.n_kv >= 1 &&
-                       it.kv_off >= 0;
-  const int p = it.p;
-  const int hk = h / (prm.Hq / prm.Hkv);
-  int NB = 0;
-  if (unit_ok)
-    for (int ki = 0; ki < it.n_kv; ++ki) NB += kblocks_of(__ldg(prm.kv_list + it.kv_off + ki), p, prm.causal, prm.nb, qb);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Ly::B_RES), 1);
+    mbar_init(bar(Ly::B_RESE), 1);
     for (int s = 0; s < Ly::NSA; ++s) {
       mbar_init(bar(Ly::B_AF + s), 1);
       mbar_init(bar(Ly::B_AE + s), 1);
@@ -632,9 +826,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar(Ly::B_DP), 1);
     mbar_init(bar(Ly::B_DS), N_EW);  // one lane of each elementwise warp
     mbar_init(bar(Ly::B_ACC), 1);
+    mbar_init(bar(Ly::B_ACCE), N_EW);
     mbar_init(bar(Ly::B_DRAIN), 1);
-    *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0 || !unit_ok) ? 1 : 0;
-    if (!unit_ok) record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_ITEM, (int32_t)blockIdx.x);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(Ly::B_UF + s), 1);
+      mbar_init(bar(Ly::B_UE + s), N_EW + 1);  // the elementwise warps and the MMA warp read a unit
+    }
+    *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0) ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -654,20 +852,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const bool run = *abort_flag == 0;
 
-  // the j-th key block of the unit: KV partition and block
-  auto block_at = [&](int j, int& kp, int& kbk) {
-    int r = j;
-    for (int ki = 0; ki < it.n_kv; ++ki) {
-      kp = __ldg(prm.kv_list + it.kv_off + ki);
-      const int n = kblocks_of(kp, p, prm.causal, prm.nb, qb);
-      if (r < n) {
-        kbk = r;
-        return;
-      }
-      r -= n;
+  // the next unit from the ring (consumers: every lane of the warp waits, one lane frees the slot)
+  int nu = 0;
+  auto take = [&](int& v, DqUnit& y, int role) -> bool {
+    const int slot = nu & 1;
+    bool r = mbar_wait_warp(bar(Ly::B_UF + slot), (uint32_t)((nu >> 1) & 1), prm.wait_limit_ns, abort_flag,
+                            prm.status, role, -1);
+    if (!r) return false;
+    v = get_unit(unit_ring + 16 * slot, y);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(Ly::B_UE + slot));
+    ++nu;
+    return true;
+  };
+  auto bad_unit = [&](int u, int role) {
+    if (lane == 0) {
+      record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, role, u);
+      *abort_flag = 1;
     }
-    kp = -1;
-    kbk = 0;
+    __syncwarp();
   };
 
   if (warp < N_EW) {
@@ -678,85 +881,123 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const uint32_t tm_dp = tmem + lane_base + 256u;  // dP, then dS (bf16)
     const uint32_t tm_dq = tmem + lane_base + 384u;
-    const int64_t q_local = (int64_t)qb * BM + row;
-    const int64_t grow = ((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + q_local;
-    const bool row_in = q_local < L;
-    const float lse2 = row_in ? __ldg(prm.lse + grow) * LOG2E : INFINITY;
-    const float dsum = row_in ? __ldg(prm.dsum + grow) : 0.f;
     bool ok = run;
-    KCursor cur;
-    cur.start(prm, it, p, qb);
-    for (int j = 0; j < NB && ok; ++j) {
-      if (j > 0) cur.step(prm, it, p, qb);
-      const int kp = cur.kp, kbk = cur.kb;
-      const int64_t kvalid = L - (int64_t)kbk * BM;
-      int hi = (int)min((int64_t)BM, kvalid);                         // keys past the partition end
-      if (prm.causal && kp == p && kbk == qb) hi = min(hi, row + 1);  // diagonal block
-      hi -= c_base;                                                   // in this half's columns
-      const bool any_mask = __any_sync(0xffffffffu, hi < 64);
-      const uint32_t tm_s = tmem + lane_base + (uint32_t)((j & 1) * 128);
-      ok = mbar_wait(bar(Ly::B_S + (j & 1)), (uint32_t)((j >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
-                     ROLE_EW, j);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      float pv[64];
-      tmem_ld32(tm_s + (uint32_t)c_base, pv);
-      tmem_ld32(tm_s + (uint32_t)c_base + 32u, pv + 32);
-      tc_wait_ld();
-      if (any_mask) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c >= hi) pv[c] = -INFINITY;
+    int v = -1;
+    DqUnit x;
+    if (ok) ok = take(v, x, ROLE_EW);
+    // LSE and D of this thread's row, loaded as soon as the unit is known and used a phase later
+    float raw_lse = 0.f, raw_d = 0.f;
+    bool row_in = false;
+    auto fetch = [&](const DqUnit& y) {
+      const int64_t ql = (int64_t)y.qb * BM + row;
+      row_in = ql < L;
+      if (row_in) {
+        const int64_t gi = ((int64_t)y.b * prm.Hq + y.h) * prm.S + (int64_t)y.it.p * L + ql;
+        raw_lse = __ldg(prm.lse + gi);
+        raw_d = __ldg(prm.dsum + gi);
       }
-      const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2);
-      const uint64_t nl2 = f2_pack(-lse2, -lse2);
-#pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), sc2, nl2), x0, x1);
-        pv[c] = fast_exp2(x0);
-        pv[c + 1] = fast_exp2(x1);
+    };
+    if (ok && v >= 0 && x.ok) fetch(x);
+    int64_t g0 = 0;  // global index of the unit's first key block
+    int k_unit = 0;
+    while (ok && v >= 0) {
+      if (!x.ok || x.NB < 1) {
+        bad_unit(v, ROLE_EW);
+        ok = false;
+        break;
       }
-      ok = mbar_wait(bar(Ly::B_DP), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, j);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      {
-        const uint64_t nd2 = f2_pack(-dsum, -dsum);
-        float dp[64];
-        tmem_ld32(tm_dp + (uint32_t)c_base, dp);
-        tmem_ld32(tm_dp + (uint32_t)c_base + 32u, dp + 32);
+      const int p = x.it.p, qb = x.qb;
+      const float lse2 = row_in ? raw_lse * LOG2E : INFINITY;
+      const float dsum = row_in ? raw_d : 0.f;
+      KCursor cur;
+      cur.start(prm, x.it, p, qb);
+      for (int j = 0; j < x.NB && ok; ++j) {
+        if (j > 0) cur.step(prm, x.it, p, qb);
+        const int64_t g = g0 + j;
+        const int kp = cur.kp, kbk = cur.kb;
+        const int64_t kvalid = L - (int64_t)kbk * BM;
+        int hi = (int)min((int64_t)BM, kvalid);                         // keys past the partition end
+        if (prm.causal && kp == p && kbk == qb) hi = min(hi, row + 1);  // diagonal block
+        hi -= c_base;                                                   // in this half's columns
+        const bool any_mask = __any_sync(0xffffffffu, hi < 64);
+        const uint32_t tm_s = tmem + lane_base + (uint32_t)((g & 1) * 128);
+        ok = mbar_wait(bar(Ly::B_S + (int)(g & 1)), (uint32_t)((g >> 1) & 1), prm.wait_limit_ns, abort_flag,
+                       prm.status, ROLE_EW, j);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        float pv[64];
+        tmem_ld32(tm_s + (uint32_t)c_base, pv);
+        tmem_ld32(tm_s + (uint32_t)c_base + 32u, pv + 32);
         tc_wait_ld();
-        uint32_t ds2[32];
+        if (any_mask) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c >= hi) pv[c] = -INFINITY;
+        }
+        const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2);
+        const uint64_t nl2 = f2_pack(-lse2, -lse2);
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          float a0, a1;
-          f2_unpack(f2_mul(f2_add(f2_pack(dp[c], dp[c + 1]), nd2), f2_pack(pv[c], pv[c + 1])), a0, a1);
-          ds2[c / 2] = pack_bf16x2(a0, a1);
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(pv[c], pv[c + 1]), sc2, nl2), x0, x1);
+          pv[c] = fast_exp2(x0);
+          pv[c + 1] = fast_exp2(x1);
         }
-        tmem_st32(tm_dp + (uint32_t)c_base, ds2);  // dS columns of this half (see packed_col)
+        ok = mbar_wait(bar(Ly::B_DP), (uint32_t)(g & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, j);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        {
+          const uint64_t nd2 = f2_pack(-dsum, -dsum);
+          float dp[64];
+          tmem_ld32(tm_dp + (uint32_t)c_base, dp);
+          tmem_ld32(tm_dp + (uint32_t)c_base + 32u, dp + 32);
+          tc_wait_ld();
+          uint32_t ds2[32];
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            float a0, a1;
+            f2_unpack(f2_mul(f2_add(f2_pack(dp[c], dp[c + 1]), nd2), f2_pack(pv[c], pv[c + 1])), a0, a1);
+            ds2[c / 2] = pack_bf16x2(a0, a1);
+          }
+          tmem_st32(tm_dp + (uint32_t)c_base, ds2);  // dS columns of this half (see packed_col)
+        }
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(Ly::B_DS));
       }
-      tc_wait_st();
+      if (!ok) break;
+      // the next unit, and its row's LSE and D, before this unit's epilogue
+      int vn = -1;
+      DqUnit xn;
+      ok = take(vn, xn, ROLE_EW);
+      if (!ok) break;
+      if (vn >= 0 && xn.ok) fetch(xn);
+      ok = mbar_wait(bar(Ly::B_ACC), (uint32_t)(k_unit & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, -1);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int64_t row0 =
+          (((int64_t)x.b * prm.Hq + x.h) * prm.n_slots + x.it.slot) * L + (int64_t)qb * BM + wq * 32;
+      const int rows_valid = (int)max((int64_t)0, min((int64_t)32, L - ((int64_t)qb * BM + wq * 32)));
+      // copy this warp's dQ columns out of TMEM, release the accumulator, then store
+      float acc[D / 2];
+#pragma unroll
+      for (int c = 0; c < D / 2; c += 32) tmem_ld32(tm_dq + (uint32_t)(hf * (D / 2) + c), acc + c);
+      tc_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(Ly::B_DS));
-    }
-    if (ok) {
-      ok = mbar_wait(bar(Ly::B_ACC), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, -1);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      tc_fence_after();
-      const int64_t row0 = (((int64_t)b * prm.Hq + h) * prm.n_slots + it.slot) * L + (int64_t)qb * BM + wq * 32;
-      const int rows_valid = (int)max((int64_t)0, min((int64_t)32, L - ((int64_t)qb * BM + wq * 32)));
-#pragma unroll 1
-      for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
-        float v[32];
-        tmem_ld32(tm_dq + (uint32_t)c, v);
-        tc_wait_ld();
-        store_rows<D>(v, prm.scale, prm.dq_part, row0, rows_valid, c, lane);
-      }
+      if (lane == 0) mbar_arrive(bar(Ly::B_ACCE));
+#pragma unroll
+      for (int c = 0; c < D / 2; c += 32)
+        store_rows<D>(*reinterpret_cast<const float(*)[32]>(acc + c), prm.scale, prm.dq_part, row0, rows_valid,
+                      hf * (D / 2) + c, lane);
+      g0 += x.NB;
+      ++k_unit;
+      v = vn;
+      x = xn;
     }
   } else if (warp == WARP_MMA) {
     // ================================================================ MMA issuer
@@ -768,14 +1009,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint64_t a_kmaj = smem_desc_sw128(sb + Ly::A0, 16u, 1024u);  // K stages
     const uint64_t a_mn = smem_desc_sw128(sb + Ly::A0, Ly::BOX, 1024u);
     const uint64_t b_kmaj = smem_desc_sw128(sb + Ly::B0, 16u, 1024u);  // V stages
-    auto issue_s = [&](int sa, int buf) {  // S = Q K^T into S buffer `buf`
-      const uint64_t kd = a_kmaj + (uint64_t)sa * TILE16;
+    auto issue_s = [&](int64_t g) {  // S(g) = Q K(g)^T into S buffer g & 1
+      const uint64_t kd = a_kmaj + (uint64_t)(g % Ly::NSA) * TILE16;
+      const uint32_t buf = (uint32_t)(g & 1);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        tc_mma_ss_warp(tmem + (uint32_t)(buf * 128), qdesc + kmaj_off<D>(kk), kd + kmaj_off<D>(kk), idesc_ss, kk > 0);
-      tc_commit_warp(bar(Ly::B_S + buf));
+        tc_mma_ss_warp(tmem + buf * 128u, qdesc + kmaj_off<D>(kk), kd + kmaj_off<D>(kk), idesc_ss, kk > 0);
+      tc_commit_warp(bar(Ly::B_S + (int)buf));
     };
-    auto issue_dp = [&](int sbb) {  // dP = dO V^T; V(j) is read by this product only
+    auto issue_dp = [&](int64_t g) {  // dP(g) = dO V(g)^T; V(g) is read by this product only
+      const int sbb = (int)(g % Ly::NSB);
       const uint64_t vd = b_kmaj + (uint64_t)sbb * TILE16;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
@@ -783,115 +1026,209 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_commit_warp(bar(Ly::B_DP));
       tc_commit_warp(bar(Ly::B_BE + sbb));
     };
-    auto issue_dq = [&](int sa, bool first) {  // dQ += dS K
-      const uint64_t kd = a_mn + (uint64_t)sa * TILE16;
+    auto issue_dq = [&](int64_t g, bool first) {  // dQ += dS(g) K(g)
+      const uint64_t kd = a_mn + (uint64_t)(g % Ly::NSA) * TILE16;
 #pragma unroll
       for (int kk = 0; kk < BM / 16; ++kk)
         tc_mma_ts_warp(tmem + 384u, tmem + 256u + packed_col(kk), kd + (uint64_t)(kk * 128), idesc_ts,
                        (!first || kk > 0) ? 1u : 0u);
+      tc_commit_warp(bar(Ly::B_AE + (int)(g % Ly::NSA)));  // K(g): read by S(g) and dQ(g)
     };
-    auto wait_a = [&](int j) {  // K(j) landed
-      return mbar_wait_warp(bar(Ly::B_AF + j % Ly::NSA), (uint32_t)((j / Ly::NSA) & 1), prm.wait_limit_ns, abort_flag,
-                            prm.status, ROLE_MMA, j);
+    auto wait_a = [&](int64_t g) {  // K(g) landed
+      return mbar_wait_warp(bar(Ly::B_AF + (int)(g % Ly::NSA)), (uint32_t)((g / Ly::NSA) & 1), prm.wait_limit_ns,
+                            abort_flag, prm.status, ROLE_MMA, (int32_t)g);
     };
-    auto wait_b = [&](int j) {  // V(j) landed
-      return mbar_wait_warp(bar(Ly::B_BF + j % Ly::NSB), (uint32_t)((j / Ly::NSB) & 1), prm.wait_limit_ns, abort_flag,
-                            prm.status, ROLE_MMA, j);
+    auto wait_b = [&](int64_t g) {  // V(g) landed
+      return mbar_wait_warp(bar(Ly::B_BF + (int)(g % Ly::NSB)), (uint32_t)((g / Ly::NSB) & 1), prm.wait_limit_ns,
+                            abort_flag, prm.status, ROLE_MMA, (int32_t)g);
     };
-    bool ok = run && NB > 0;
-    if (ok) ok = mbar_wait_warp(bar(Ly::B_RES), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, -1);
-    if (ok) ok = wait_a(0);
-    if (ok) {
+    int nres = 0;
+    // S(0), dP(0) and S(1) of a unit whose first block is g: issued as soon as its resident Q and
+    // dO have landed (for every unit but the first, after the previous unit's last dQ)
+    auto start_unit = [&](const DqUnit& y, int64_t g) -> bool {
+      if (!mbar_wait_warp(bar(Ly::B_RES), (uint32_t)(nres & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                          ROLE_MMA, -1))
+        return false;
+      ++nres;
+      if (!wait_a(g)) return false;
       tc_fence_after();
-      issue_s(0, 0);
-      ok = wait_b(0);
+      issue_s(g);
+      if (!wait_b(g)) return false;
+      tc_fence_after();
+      issue_dp(g);
+      if (y.NB == 1) tc_commit_warp(bar(Ly::B_RESE));  // the unit's last S and dP are issued
+      if (y.NB > 1) {
+        if (!wait_a(g + 1)) return false;
+        tc_fence_after();
+        issue_s(g + 1);
+      }
+      return true;
+    };
+    bool ok = run;
+    int v = -1;
+    DqUnit x;
+    if (ok) ok = take(v, x, ROLE_MMA);
+    if (ok && v >= 0) {
+      if (!x.ok || x.NB < 1) {
+        bad_unit(v, ROLE_MMA);
+        ok = false;
+      } else {
+        ok = start_unit(x, 0);
+      }
     }
-    if (ok) {
-      tc_fence_after();
-      issue_dp(0);
-      if (NB > 1) {
-        ok = wait_a(1);
-        if (ok) {
+    int64_t g0 = 0;
+    int k_unit = 0;
+    while (ok && v >= 0) {
+      const int NB = x.NB;
+      for (int j = 0; j < NB && ok; ++j) {
+        const int64_t g = g0 + j;
+        // dS(g) is in TMEM, and S(g) has been read, so its buffer is free for S(g+2).  (One barrier per
+        // block, passed in order: a second "S read" barrier could complete for block g+1, whose S is
+        // issued two blocks ahead, before this warp observed block g -- two phases ahead of its
+        // parity wait.)
+        ok = mbar_wait_warp(bar(Ly::B_DS), (uint32_t)(g & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
+        if (!ok) break;
+        if (j == 0 && k_unit > 0) {  // the previous unit's dQ has been copied out of TMEM
+          ok = mbar_wait_warp(bar(Ly::B_ACCE), (uint32_t)((k_unit - 1) & 1), prm.wait_limit_ns, abort_flag,
+                              prm.status, ROLE_MMA, -1);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        issue_dq(g, j == 0);
+        if (j + 1 == NB) tc_commit_warp(bar(Ly::B_ACC));
+        if (j + 1 < NB) {
+          ok = wait_b(g + 1);
+          if (!ok) break;
           tc_fence_after();
-          issue_s(1, 1);
+          issue_dp(g + 1);
+          if (j + 2 == NB) tc_commit_warp(bar(Ly::B_RESE));  // the unit's last S and dP are issued
+        }
+        if (j + 2 < NB) {
+          ok = wait_a(g + 2);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(g + 2);
         }
       }
-    }
-    for (int j = 0; j < NB && ok; ++j) {
-      // dS(j) is in TMEM, and S(j) has been read, so its buffer is free for S(j+2).  (One barrier per
-      // block, passed in order: a second "S read" barrier could complete for block j+1, whose S is
-      // issued two blocks ahead, before this warp observed block j -- two phases ahead of its
-      // parity wait.)
-      ok = mbar_wait_warp(bar(Ly::B_DS), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
       if (!ok) break;
-      tc_fence_after();
-      issue_dq(j % Ly::NSA, j == 0);
-      tc_commit_warp(bar(Ly::B_AE + j % Ly::NSA));  // K(j): read by S(j) and dQ(j)
-      if (j + 1 < NB) {
-        ok = wait_b(j + 1);
-        if (!ok) break;
-        tc_fence_after();
-        issue_dp((j + 1) % Ly::NSB);
+      int vn = -1;
+      ok = take(vn, x, ROLE_MMA);
+      if (!ok) break;
+      g0 += NB;
+      ++k_unit;
+      v = vn;
+      if (v < 0) break;
+      if (!x.ok || x.NB < 1) {
+        bad_unit(v, ROLE_MMA);
+        ok = false;
+        break;
       }
-      if (j + 2 < NB) {
-        ok = wait_a(j + 2);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s((j + 2) % Ly::NSA, j & 1);
-      }
+      ok = start_unit(x, g0);
     }
-    if (ok) tc_commit_warp(bar(Ly::B_ACC));
+    // exit-path drain: every MMA issued completes before TMEM is freed
     tc_commit_warp(bar(Ly::B_DRAIN));
     mbar_drain(bar(Ly::B_DRAIN), 0u, DRAIN_NS);
   } else if (warp == WARP_LOAD && lane == 0) {
     // ================================================================ producer
-    bool ok = run && NB > 0;
-    const int64_t qrow = ((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + (int64_t)qb * BM;
-    const int64_t kvbase = ((int64_t)b * prm.Hkv + hk) * prm.S;
-    if (ok) {
+    bool ok = run;
+    int np = 0;  // units published
+    auto publish = [&](DqUnit& y) -> int {
+      const int slot = np & 1;
+      ok = mbar_wait(bar(Ly::B_UE + slot), (uint32_t)(((np >> 1) & 1) ^ 1), prm.wait_limit_ns, abort_flag,
+                     prm.status, ROLE_LOAD, -1);
+      if (!ok) return -1;
+      int u = (int)atomicAdd(prm.counter_dq, 1u);
+      if (u >= prm.n_dq_units) u = -1;
+      if (u >= 0) y = dq_unit(u, prm);
+      put_unit(unit_ring + 16 * slot, u, y);
+      mbar_arrive(bar(Ly::B_UF + slot));
+      ++np;
+      return u;
+    };
+    int nres = 0;
+    int64_t ga = 0, gb = 0;  // K and V blocks issued
+    DqUnit x, y;
+    int u = ok ? publish(x) : -1;
+    while (ok && u >= 0) {
+      if (!x.ok || x.NB < 1) {
+        record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_LOAD, u);
+        *abort_flag = 1;
+        break;
+      }
+      // publish the following unit now and pull its Q, dO rows and first K, V block into L2
+      const int un = publish(y);
+      if (!ok) break;
+      if (un >= 0) {
+        if (y.ok) {
+          const int64_t qn = ((int64_t)y.b * prm.Hq + y.h) * prm.S + (int64_t)y.it.p * L + (int64_t)y.qb * BM;
+          for (int c = 0; c < D / 64; ++c) {
+            tma_prefetch_l2_2d(&tmQ, c * 64, (int32_t)qn);
+            tma_prefetch_l2_2d(&tmG, c * 64, (int32_t)qn);
+          }
+          const int kn = __ldg(prm.kv_list + y.it.kv_off);
+          if (kn >= 0 && kn < prm.P) {
+            const int64_t krn = ((int64_t)y.b * prm.Hkv + y.hk) * prm.S + (int64_t)kn * L;
+            for (int c = 0; c < D / 64; ++c) {
+              tma_prefetch_l2_2d(&tmK, c * 64, (int32_t)krn);
+              tma_prefetch_l2_2d(&tmV, c * 64, (int32_t)krn);
+            }
+          }
+        }
+      }
+      // resident Q and dO: the previous unit's last S and dP products must be done with them
+      ok = mbar_wait(bar(Ly::B_RESE), (uint32_t)((nres & 1) ^ 1), prm.wait_limit_ns, abort_flag, prm.status,
+                     ROLE_LOAD, u);
+      if (!ok) break;
+      const int64_t qrow = ((int64_t)x.b * prm.Hq + x.h) * prm.S + (int64_t)x.it.p * L + (int64_t)x.qb * BM;
       mbar_expect_tx(bar(Ly::B_RES), 2 * Ly::TILE);
       for (int c = 0; c < D / 64; ++c) {
         tma_load_2d(sb + Ly::RES0 + (uint32_t)c * Ly::BOX, &tmQ, c * 64, (int32_t)qrow, bar(Ly::B_RES));
         tma_load_2d(sb + Ly::RES1 + (uint32_t)c * Ly::BOX, &tmG, c * 64, (int32_t)qrow, bar(Ly::B_RES));
       }
+      ++nres;
+      const int64_t kvbase = ((int64_t)x.b * prm.Hkv + x.hk) * prm.S;
+      KCursor cur;
+      cur.start(prm, x.it, x.it.p, x.qb);
+      for (int j = 0; j < x.NB && ok; ++j) {
+        if (j > 0) cur.step(prm, x.it, x.it.p, x.qb);
+        if (cur.kp < 0 || cur.kp >= prm.P) {
+          record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_LOAD, u);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        const int32_t krow = (int32_t)(kvbase + (int64_t)cur.kp * L + (int64_t)cur.kb * BM);
+        const int sa = (int)(ga % Ly::NSA), sbb = (int)(gb % Ly::NSB);
+        if (ga >= Ly::NSA) {
+          ok = mbar_wait(bar(Ly::B_AE + sa), (uint32_t)((ga / Ly::NSA - 1) & 1), prm.wait_limit_ns, abort_flag,
+                         prm.status, ROLE_LOAD, j);
+          if (!ok) break;
+        }
+        mbar_expect_tx(bar(Ly::B_AF + sa), Ly::TILE);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(sb + Ly::A0 + (uint32_t)sa * Ly::TILE + (uint32_t)c * Ly::BOX, &tmK, c * 64, krow,
+                      bar(Ly::B_AF + sa));
+        ++ga;
+        if (gb >= Ly::NSB) {
+          ok = mbar_wait(bar(Ly::B_BE + sbb), (uint32_t)((gb / Ly::NSB - 1) & 1), prm.wait_limit_ns, abort_flag,
+                         prm.status, ROLE_LOAD, j);
+          if (!ok) break;
+        }
+        mbar_expect_tx(bar(Ly::B_BF + sbb), Ly::TILE);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(sb + Ly::B0 + (uint32_t)sbb * Ly::TILE + (uint32_t)c * Ly::BOX, &tmV, c * 64, krow,
+                      bar(Ly::B_BF + sbb));
+        ++gb;
+      }
+      u = un;
+      x = y;
     }
-    int issued_a = 0, issued_b = 0;
-    for (int j = 0; j < NB && ok; ++j) {
-      int kp, kbk;
-      block_at(j, kp, kbk);
-      if (kp < 0 || kp >= prm.P) {
-        record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_LOAD, (int32_t)blockIdx.x);
-        *abort_flag = 1;
-        break;
-      }
-      const int32_t krow = (int32_t)(kvbase + (int64_t)kp * L + (int64_t)kbk * BM);
-      const int sa = j % Ly::NSA, sbb = j % Ly::NSB;
-      if (j >= Ly::NSA) {
-        ok = mbar_wait(bar(Ly::B_AE + sa), (uint32_t)((j / Ly::NSA - 1) & 1), prm.wait_limit_ns, abort_flag,
-                       prm.status, ROLE_LOAD, j);
-        if (!ok) break;
-      }
-      mbar_expect_tx(bar(Ly::B_AF + sa), Ly::TILE);
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_2d(sb + Ly::A0 + (uint32_t)sa * Ly::TILE + (uint32_t)c * Ly::BOX, &tmK, c * 64, krow,
-                    bar(Ly::B_AF + sa));
-      ++issued_a;
-      if (j >= Ly::NSB) {
-        ok = mbar_wait(bar(Ly::B_BE + sbb), (uint32_t)((j / Ly::NSB - 1) & 1), prm.wait_limit_ns, abort_flag,
-                       prm.status, ROLE_LOAD, j);
-        if (!ok) break;
-      }
-      mbar_expect_tx(bar(Ly::B_BF + sbb), Ly::TILE);
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_2d(sb + Ly::B0 + (uint32_t)sbb * Ly::TILE + (uint32_t)c * Ly::BOX, &tmV, c * 64, krow,
-                    bar(Ly::B_BF + sbb));
-      ++issued_b;
-    }
-    if (run && NB > 0) mbar_drain(bar(Ly::B_RES), 0u, DRAIN_NS);
-    for (int j = (issued_a > Ly::NSA ? issued_a - Ly::NSA : 0); j < issued_a; ++j)
-      mbar_drain(bar(Ly::B_AF + j % Ly::NSA), (uint32_t)((j / Ly::NSA) & 1), DRAIN_NS);
-    for (int j = (issued_b > Ly::NSB ? issued_b - Ly::NSB : 0); j < issued_b; ++j)
-      mbar_drain(bar(Ly::B_BF + j % Ly::NSB), (uint32_t)((j / Ly::NSB) & 1), DRAIN_NS);
+    // exit-path drain: every load issued lands before the CTA exits
+    if (nres > 0) mbar_drain(bar(Ly::B_RES), (uint32_t)((nres - 1) & 1), DRAIN_NS);
+    for (int64_t j = (ga > Ly::NSA ? ga - Ly::NSA : 0); j < ga; ++j)
+      mbar_drain(bar(Ly::B_AF + (int)(j % Ly::NSA)), (uint32_t)((j / Ly::NSA) & 1), DRAIN_NS);
+    for (int64_t j = (gb > Ly::NSB ? gb - Ly::NSB : 0); j < gb; ++j)
+      mbar_drain(bar(Ly::B_BF + (int)(j % Ly::NSB)), (uint32_t)((j / Ly::NSB) & 1), DRAIN_NS);
   }
 
   tc_fence_before();
@@ -966,6 +1303,10 @@ static int launch(const BwdArgs& a, void* stream, std::string* err) {
   prm.dk_part = a.dk_part;
   prm.dv_part = a.dv_part;
   prm.status = a.status;
+  prm.counter_dq = a.counters;
+  prm.counter_kv = a.counters + 64;  // the second 256-byte counter slot
+  prm.n_dq_units = (int32_t)dq_units;
+  prm.n_kv_units = (int32_t)kv_units;
   prm.S = a.S;
   prm.L = a.L;
   prm.B = a.B;
@@ -989,11 +1330,21 @@ static int launch(const BwdArgs& a, void* stream, std::string* err) {
     *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
     return (int)e;
   }
+  // persistent grids: one CTA per SM, units handed out by the counters
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess || sms < 1) {
+    *err = std::string("SM count: ") + cudaGetErrorString(e);
+    return (int)(e != cudaSuccess ? e : cudaErrorInvalidDevice);
+  }
   cudaStream_t st = (cudaStream_t)stream;
   if (kv_units > 0)
-    bwd_dkdv_kernel<D><<<dim3((unsigned)kv_units), dim3(NUM_THREADS), Layout<D>::ALLOC, st>>>(mq, mk, mv, mg, prm);
+    bwd_dkdv_kernel<D><<<dim3((unsigned)std::min<int64_t>(kv_units, sms)), dim3(NUM_THREADS), Layout<D>::ALLOC, st>>>(
+        mq, mk, mv, mg, prm);
   if (dq_units > 0)
-    bwd_dq_kernel<D><<<dim3((unsigned)dq_units), dim3(NUM_THREADS), Layout<D>::ALLOC, st>>>(mq, mk, mv, mg, prm);
+    bwd_dq_kernel<D><<<dim3((unsigned)std::min<int64_t>(dq_units, sms)), dim3(NUM_THREADS), Layout<D>::ALLOC, st>>>(
+        mq, mk, mv, mg, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) *err = std::string("tile_bwd_tc launch: ") + cudaGetErrorString(e);
   return (int)e;
