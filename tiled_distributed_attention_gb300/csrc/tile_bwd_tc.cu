@@ -6,12 +6,20 @@
 // §"Mesh-Attention：从一维'环'到二维'网'"), with the forward's global LSE and D_i = dO_i . O_i:
 //   P_ij = exp(s_ij - LSE_i),  dP_ij = dO_i . v_j,  dS_ij = P_ij (dP_ij - D_i),
 //   dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j.
-// Two kernels; one CTA owns one 128-row tile of one unit (no persistence) with 10 warps:
-//   warps 0-7  elementwise: two warps per TMEM lane quadrant, one thread per TMEM lane (a key row
-//              in dkdv, a query row in dq), each warp taking 64 of the block's 128 columns
-//   warp 8     MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M = N = 128, K = 16, issued by an
-//              elected lane of the converged warp; completion by tcgen05.commit
-//   warp 9     producer: TMA loads of 128 x 64 bf16 boxes with 128-byte swizzle
+// Two persistent kernels: one CTA per SM takes units (one 128-row tile each) from a global
+// counter; the producer decodes a unit and publishes it through a two-entry shared-memory ring.
+// 16 warps in four warpgroups, registers rebalanced with setmaxnreg:
+//   warps 0-7   elementwise: two warps per TMEM lane quadrant, one thread per TMEM lane (a key row
+//               in dkdv, a query row in dq), each warp taking 64 of the block's 128 columns
+//   warp 8      MMA issuer: tcgen05.mma.cta_group::1.kind::f16, M = N = 128, K = 16, issued by an
+//               elected lane of the converged warp; completion by tcgen05.commit
+//   warp 9      producer: TMA loads of 128 x 64 bf16 boxes with 128-byte swizzle
+//   warps 10-11 idle
+//   warps 12-15 epilogue: one per TMEM lane quadrant; copies a unit's accumulators out of TMEM
+//               and stores its partial rows while the other roles run the next unit
+// Across units: the next unit's resident block loads as soon as the last products reading the
+// current one have completed, its first products are issued right after the current unit's
+// last accumulation, and an accumulator is overwritten only after the epilogue has copied it.
 //
 // dkdv (unit = KV slot, batch, KV head, 128-key block): K and V stay in shared memory; Q and dO
 // blocks of the slot's query rows (over the KV head's query heads) stream through three and two
@@ -43,10 +51,17 @@ namespace mesh {
 namespace btc {
 
 constexpr int BM = 128;  // rows per tile = TMEM lanes = keys / queries per block
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 512;
 constexpr int N_EW = 8;  // elementwise warps: two per TMEM lane quadrant, 64 columns each
 constexpr int WARP_MMA = 8;
 constexpr int WARP_LOAD = 9;
+constexpr int WARP_EPI = 12;  // warps 12-15: epilogue, one per TMEM lane quadrant (warps 10-11 idle)
+constexpr int N_EPI = 4;
+// Register budgets after setmaxnreg, per warpgroup: elementwise (warps 0-7), MMA / producer
+// (8-11), epilogue (12-15).  They add up to the 512 x 128 registers of the launch; the launcher
+// checks the kernels' register count against that before launching.
+constexpr int EW_REGS = 168, MMA_REGS = 104, EPI_REGS = 72;
+static_assert(2 * 128 * EW_REGS + 128 * MMA_REGS + 128 * EPI_REGS <= NUM_THREADS * 128, "register split");
 // The bf16 P / dS written back into TMEM by column half `hf` land in packed columns
 // [64 hf, 64 hf + 32) of their region -- inside the half's own input columns, so the halves never
 // overwrite values the other still has to read -- and the MMAs that take them as A read K-step kk
@@ -54,7 +69,7 @@ constexpr int WARP_LOAD = 9;
 __device__ __forceinline__ uint32_t packed_col(int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); }
 constexpr int64_t DRAIN_NS = 200000000;
 constexpr float LOG2E = 1.4426950408889634f;
-constexpr int ROLE_EW = 1, ROLE_MMA = 2, ROLE_LOAD = 3, ROLE_ITEM = 4;
+constexpr int ROLE_EW = 1, ROLE_MMA = 2, ROLE_LOAD = 3, ROLE_ITEM = 4, ROLE_EPI = 5;
 
 struct Params {
   const DevItem* items;
@@ -94,7 +109,8 @@ struct Layout {
   static constexpr int B_RES = 0, B_AF = 1, B_AE = B_AF + NSA, B_BF = B_AE + NSA, B_BE = B_BF + NSB,
                        B_S = B_BE + NSB, B_DP = B_S + 2, B_P = B_DP + 1, B_DS = B_P + 1, B_ACC = B_DS + 1,
                        B_DRAIN = B_ACC + 1, B_VEC = B_DRAIN + 1, B_RESE = B_VEC + 2, B_ACCE = B_RESE + 1,
-                       B_UF = B_ACCE + 1, B_UE = B_UF + 2, NBARS = B_UE + 2;
+                       B_UF = B_ACCE + 1, B_UE = B_UF + 2, B_ACC2 = B_UE + 2, B_ACCE2 = B_ACC2 + 1,
+                       NBARS = B_ACCE2 + 1;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag
   static constexpr uint32_t RING_OFF = MISC_OFF + 16;         // unit ring: 2 decoded units, 16 ints each
   static constexpr uint32_t TOTAL = RING_OFF + 2 * 64;
@@ -292,13 +308,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar(Ly::B_P), N_EW);  // one lane of each elementwise warp
     mbar_init(bar(Ly::B_DS), N_EW);
     mbar_init(bar(Ly::B_ACC), 1);
-    mbar_init(bar(Ly::B_ACCE), N_EW);
+    mbar_init(bar(Ly::B_ACCE), N_EPI);  // one lane of each epilogue warp
+    mbar_init(bar(Ly::B_ACC2), 1);
+    mbar_init(bar(Ly::B_ACCE2), N_EPI);
     mbar_init(bar(Ly::B_DRAIN), 1);
     mbar_init(bar(Ly::B_VEC), BM);  // every elementwise thread has written its LSE / D value
     mbar_init(bar(Ly::B_VEC + 1), BM);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(Ly::B_UF + s), 1);
-      mbar_init(bar(Ly::B_UE + s), N_EW + 1);  // the elementwise warps and the MMA warp read a unit
+      mbar_init(bar(Ly::B_UE + s), N_EW + 1 + N_EPI);  // elementwise, MMA and epilogue warps read a unit
     }
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0) ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -342,14 +360,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp < N_EW) {
     // ================================================================ elementwise
+    regs_inc<EW_REGS>();
     const int wq = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
     const int row = wq * 32 + lane;           // TMEM lane = key row within the block
     const int c_base = hf * 64;               // this warp's query columns [c_base, c_base + 64)
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const uint32_t tm_s = tmem + lane_base;           // S^T, then P^T (bf16)
     const uint32_t tm_dp = tmem + lane_base + 128u;   // dP^T, then dS^T (bf16)
-    const uint32_t tm_dv = tmem + lane_base + 256u;
-    const uint32_t tm_dk = tmem + lane_base + 256u + (uint32_t)D;
     bool ok = run;
     // LSE and D of query column `row` for the next block, loaded raw one block ahead by the first
     // column half and only used (scaled, published) at the top of the next iteration, so that the
@@ -379,7 +396,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     int64_t g0 = 0;  // global index of the unit's first query block
-    int k_unit = 0;
     while (ok && v >= 0) {
       if (!x.ok || x.NBQ < 1) {
         bad_unit(v, ROLE_EW);
@@ -474,7 +490,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) mbar_arrive(bar(Ly::B_DS));
       }
       if (!ok) break;
-      // the next unit, and its first block's LSE and D, before this unit's epilogue
+      // the next unit, and its first block's LSE and D (the epilogue warps drain this one)
       int vn = -1;
       KvUnit xn;
       ok = take(vn, xn, ROLE_EW);
@@ -485,40 +501,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (hf == 0) fetch(xn, cur);
         }
       }
-      // ---- epilogue: this half's columns of the dV and dK rows of this key block
-      ok = mbar_wait(bar(Ly::B_ACC), (uint32_t)(k_unit & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, -1);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const int64_t row0 =
-          (((int64_t)x.b * prm.Hkv + x.hk) * prm.n_kv_slots + x.it.slot) * L + (int64_t)kb * BM + wq * 32;
-      const int rows_valid = (int)max((int64_t)0, min((int64_t)32, L - ((int64_t)kb * BM + wq * 32)));
-      // copy both accumulators' columns out of TMEM in two halves (registers), releasing TMEM
-      // after the second, then store
-      float acc[D / 2];
-#pragma unroll
-      for (int c = 0; c < D / 2; c += 32) tmem_ld32(tm_dv + (uint32_t)(hf * (D / 2) + c), acc + c);
-      tc_wait_ld();
-#pragma unroll
-      for (int c = 0; c < D / 2; c += 32)
-        store_rows<D>(*reinterpret_cast<const float(*)[32]>(acc + c), 1.f, prm.dv_part, row0, rows_valid,
-                      hf * (D / 2) + c, lane);
-#pragma unroll
-      for (int c = 0; c < D / 2; c += 32) tmem_ld32(tm_dk + (uint32_t)(hf * (D / 2) + c), acc + c);
-      tc_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(Ly::B_ACCE));
-#pragma unroll
-      for (int c = 0; c < D / 2; c += 32)
-        store_rows<D>(*reinterpret_cast<const float(*)[32]>(acc + c), prm.scale, prm.dk_part, row0, rows_valid,
-                      hf * (D / 2) + c, lane);
       g0 += NBQ;
-      ++k_unit;
       v = vn;
       x = xn;
     }
-  } else if (warp == WARP_MMA) {
+  } else if (warp < WARP_EPI) {
+    regs_dec<MMA_REGS>();
+    if (warp == WARP_MMA) {
     // ================================================================ MMA issuer
     constexpr uint32_t idesc_ss = idesc_bf16_f32(BM, BM, false);  // S^T, dP^T: K-major A and B
     constexpr uint32_t idesc_ts = idesc_bf16_f32(BM, D, true);    // dV, dK: B MN-major
@@ -606,13 +595,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int64_t gi = g0 + i;
         ok = mbar_wait_warp(bar(Ly::B_P), (uint32_t)(gi & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, i);
         if (!ok) break;
-        if (i == 0 && k_unit > 0) {  // the previous unit's dV and dK have been copied out of TMEM
+        if (i == 0 && k_unit > 0) {  // the previous unit's dV has been copied out of TMEM
           ok = mbar_wait_warp(bar(Ly::B_ACCE), (uint32_t)((k_unit - 1) & 1), prm.wait_limit_ns, abort_flag,
                               prm.status, ROLE_MMA, -1);
           if (!ok) break;
         }
         tc_fence_after();
         issue_dv(gi, i == 0);
+        if (i + 1 == NBQ) tc_commit_warp(bar(Ly::B_ACC));  // dV complete: the epilogue may drain it
         if (i + 1 < NBQ) {
           ok = wait_a(gi + 1);
           if (!ok) break;
@@ -621,9 +611,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         ok = mbar_wait_warp(bar(Ly::B_DS), (uint32_t)(gi & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, i);
         if (!ok) break;
+        if (i == 0 && k_unit > 0) {  // the previous unit's dK has been copied out of TMEM
+          ok = mbar_wait_warp(bar(Ly::B_ACCE2), (uint32_t)((k_unit - 1) & 1), prm.wait_limit_ns, abort_flag,
+                              prm.status, ROLE_MMA, -1);
+          if (!ok) break;
+        }
         tc_fence_after();
         issue_dk(gi, i == 0);
-        if (i + 1 == NBQ) tc_commit_warp(bar(Ly::B_ACC));
+        if (i + 1 == NBQ) tc_commit_warp(bar(Ly::B_ACC2));  // dK complete
         if (i + 1 < NBQ) {
           ok = wait_b(gi + 1);
           if (!ok) break;
@@ -650,7 +645,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // exit-path drain: every MMA issued completes before TMEM is freed
     tc_commit_warp(bar(Ly::B_DRAIN));
     mbar_drain(bar(Ly::B_DRAIN), 0u, DRAIN_NS);
-  } else if (warp == WARP_LOAD && lane == 0) {
+    } else if (warp == WARP_LOAD && lane == 0) {
     // ================================================================ producer
     bool ok = run;
     int np = 0;  // units published
@@ -743,6 +738,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_drain(bar(Ly::B_AF + (int)(j % Ly::NSA)), (uint32_t)((j / Ly::NSA) & 1), DRAIN_NS);
     for (int64_t j = (gb > Ly::NSB ? gb - Ly::NSB : 0); j < gb; ++j)
       mbar_drain(bar(Ly::B_BF + (int)(j % Ly::NSB)), (uint32_t)((j / Ly::NSB) & 1), DRAIN_NS);
+    }
+  } else {
+    // ================================================================ epilogue
+    // Drains the accumulators of each unit while the other roles run the next one: dV as soon
+    // as its last product completes, then dK; each is released (so the next unit may overwrite
+    // it) once its last TMEM load has completed, before the stores of that chunk.
+    regs_dec<EPI_REGS>();
+    const int wq = warp & 3;  // TMEM lane quadrant
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t tm_dv = tmem + lane_base + 256u;
+    const uint32_t tm_dk = tmem + lane_base + 256u + (uint32_t)D;
+    bool ok = run;
+    int v = -1, k_unit = 0;
+    KvUnit x;
+    if (ok) ok = take(v, x, ROLE_EPI);
+    while (ok && v >= 0) {
+      if (!x.ok || x.NBQ < 1) {
+        bad_unit(v, ROLE_EPI);
+        ok = false;
+        break;
+      }
+      const int64_t row0 =
+          (((int64_t)x.b * prm.Hkv + x.hk) * prm.n_kv_slots + x.it.slot) * L + (int64_t)x.kb * BM + wq * 32;
+      const int rows_valid = (int)max((int64_t)0, min((int64_t)32, L - ((int64_t)x.kb * BM + wq * 32)));
+      for (int which = 0; which < 2 && ok; ++which) {
+        ok = mbar_wait_warp(bar(which ? Ly::B_ACC2 : Ly::B_ACC), (uint32_t)(k_unit & 1), prm.wait_limit_ns, abort_flag,
+                            prm.status, ROLE_EPI, -1);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tm = which ? tm_dk : tm_dv;
+        float* dst = which ? prm.dk_part : prm.dv_part;
+        const float mul = which ? prm.scale : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          float t[32];
+          tmem_ld32(tm + (uint32_t)c, t);
+          tc_wait_ld();
+          if (c + 32 == D) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(which ? Ly::B_ACCE2 : Ly::B_ACCE));
+          }
+          store_rows<D>(t, mul, dst, row0, rows_valid, c, lane);
+        }
+      }
+      if (!ok) break;
+      ++k_unit;
+      ok = take(v, x, ROLE_EPI);
+    }
   }
 
   tc_fence_before();
@@ -826,11 +870,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar(Ly::B_DP), 1);
     mbar_init(bar(Ly::B_DS), N_EW);  // one lane of each elementwise warp
     mbar_init(bar(Ly::B_ACC), 1);
-    mbar_init(bar(Ly::B_ACCE), N_EW);
+    mbar_init(bar(Ly::B_ACCE), N_EPI);  // one lane of each epilogue warp
     mbar_init(bar(Ly::B_DRAIN), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(Ly::B_UF + s), 1);
-      mbar_init(bar(Ly::B_UE + s), N_EW + 1);  // the elementwise warps and the MMA warp read a unit
+      mbar_init(bar(Ly::B_UE + s), N_EW + 1 + N_EPI);  // elementwise, MMA and epilogue warps read a unit
     }
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0) ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -875,12 +919,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp < N_EW) {
     // ================================================================ elementwise
+    regs_inc<EW_REGS>();
     const int wq = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
     const int row = wq * 32 + lane;           // TMEM lane = query row within the block
     const int c_base = hf * 64;               // this warp's key columns [c_base, c_base + 64)
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const uint32_t tm_dp = tmem + lane_base + 256u;  // dP, then dS (bf16)
-    const uint32_t tm_dq = tmem + lane_base + 384u;
     bool ok = run;
     int v = -1;
     DqUnit x;
@@ -899,7 +943,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     if (ok && v >= 0 && x.ok) fetch(x);
     int64_t g0 = 0;  // global index of the unit's first key block
-    int k_unit = 0;
     while (ok && v >= 0) {
       if (!x.ok || x.NB < 1) {
         bad_unit(v, ROLE_EW);
@@ -969,37 +1012,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) mbar_arrive(bar(Ly::B_DS));
       }
       if (!ok) break;
-      // the next unit, and its row's LSE and D, before this unit's epilogue
+      // the next unit, and its row's LSE and D (the epilogue warps drain this one)
       int vn = -1;
       DqUnit xn;
       ok = take(vn, xn, ROLE_EW);
       if (!ok) break;
       if (vn >= 0 && xn.ok) fetch(xn);
-      ok = mbar_wait(bar(Ly::B_ACC), (uint32_t)(k_unit & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, -1);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const int64_t row0 =
-          (((int64_t)x.b * prm.Hq + x.h) * prm.n_slots + x.it.slot) * L + (int64_t)qb * BM + wq * 32;
-      const int rows_valid = (int)max((int64_t)0, min((int64_t)32, L - ((int64_t)qb * BM + wq * 32)));
-      // copy this warp's dQ columns out of TMEM, release the accumulator, then store
-      float acc[D / 2];
-#pragma unroll
-      for (int c = 0; c < D / 2; c += 32) tmem_ld32(tm_dq + (uint32_t)(hf * (D / 2) + c), acc + c);
-      tc_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(Ly::B_ACCE));
-#pragma unroll
-      for (int c = 0; c < D / 2; c += 32)
-        store_rows<D>(*reinterpret_cast<const float(*)[32]>(acc + c), prm.scale, prm.dq_part, row0, rows_valid,
-                      hf * (D / 2) + c, lane);
       g0 += x.NB;
-      ++k_unit;
       v = vn;
       x = xn;
     }
-  } else if (warp == WARP_MMA) {
+  } else if (warp < WARP_EPI) {
+    regs_dec<MMA_REGS>();
+    if (warp == WARP_MMA) {
     // ================================================================ MMA issuer
     constexpr uint32_t idesc_ss = idesc_bf16_f32(BM, BM, false);  // S = Q K^T, dP = dO V^T
     constexpr uint32_t idesc_ts = idesc_bf16_f32(BM, D, true);    // dQ += dS K, K MN-major
@@ -1128,7 +1153,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // exit-path drain: every MMA issued completes before TMEM is freed
     tc_commit_warp(bar(Ly::B_DRAIN));
     mbar_drain(bar(Ly::B_DRAIN), 0u, DRAIN_NS);
-  } else if (warp == WARP_LOAD && lane == 0) {
+    } else if (warp == WARP_LOAD && lane == 0) {
     // ================================================================ producer
     bool ok = run;
     int np = 0;  // units published
@@ -1229,6 +1254,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_drain(bar(Ly::B_AF + (int)(j % Ly::NSA)), (uint32_t)((j / Ly::NSA) & 1), DRAIN_NS);
     for (int64_t j = (gb > Ly::NSB ? gb - Ly::NSB : 0); j < gb; ++j)
       mbar_drain(bar(Ly::B_BF + (int)(j % Ly::NSB)), (uint32_t)((j / Ly::NSB) & 1), DRAIN_NS);
+    }
+  } else {
+    // ================================================================ epilogue
+    // Drains each unit's dQ while the other roles run the next one, releasing it (so the next
+    // unit may overwrite it) once its last TMEM load has completed.
+    regs_dec<EPI_REGS>();
+    const int wq = warp & 3;  // TMEM lane quadrant
+    const uint32_t tm_dq = tmem + ((uint32_t)(wq * 32) << 16) + 384u;
+    bool ok = run;
+    int v = -1, k_unit = 0;
+    DqUnit x;
+    if (ok) ok = take(v, x, ROLE_EPI);
+    while (ok && v >= 0) {
+      if (!x.ok || x.NB < 1) {
+        bad_unit(v, ROLE_EPI);
+        ok = false;
+        break;
+      }
+      const int64_t row0 =
+          (((int64_t)x.b * prm.Hq + x.h) * prm.n_slots + x.it.slot) * L + (int64_t)x.qb * BM + wq * 32;
+      const int rows_valid = (int)max((int64_t)0, min((int64_t)32, L - ((int64_t)x.qb * BM + wq * 32)));
+      ok = mbar_wait_warp(bar(Ly::B_ACC), (uint32_t)(k_unit & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                          ROLE_EPI, -1);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        float t[32];
+        tmem_ld32(tm_dq + (uint32_t)c, t);
+        tc_wait_ld();
+        if (c + 32 == D) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(Ly::B_ACCE));
+        }
+        store_rows<D>(t, prm.scale, prm.dq_part, row0, rows_valid, c, lane);
+      }
+      ++k_unit;
+      ok = take(v, x, ROLE_EPI);
+    }
   }
 
   tc_fence_before();
@@ -1329,6 +1394,21 @@ static int launch(const BwdArgs& a, void* stream, std::string* err) {
   if (e != cudaSuccess) {
     *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
     return (int)e;
+  }
+  // setmaxnreg hands registers between warpgroups within the launch's pool: the split must fit
+  // the registers each kernel is launched with, or a raising warpgroup would wait forever
+  for (const void* fn : {(const void*)bwd_dkdv_kernel<D>, (const void*)bwd_dq_kernel<D>}) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) {
+      *err = std::string("cudaFuncGetAttributes: ") + cudaGetErrorString(e);
+      return (int)e;
+    }
+    if (fa.numRegs * NUM_THREADS < 2 * 128 * EW_REGS + 128 * MMA_REGS + 128 * EPI_REGS) {
+      *err = "backward kernels built with " + std::to_string(fa.numRegs) +
+             " registers per thread, fewer than their warpgroups' register split needs";
+      return (int)cudaErrorInvalidConfiguration;
+    }
   }
   // persistent grids: one CTA per SM, units handed out by the counters
   int dev = 0, sms = 0;
