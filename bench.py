@@ -385,6 +385,11 @@ def main():
         plan = m.mesh_attn_plan_create_ring(w.S, w.P, w.causal)
     else:
         plan = m.mesh_attn_plan_create(w.S, w.P, w.causal, w.kvr, w.greedy)
+    # host time to build the plan (tiles, greedy order, slot lists): reported, not in the step
+    t_plan = time.perf_counter()
+    (m.mesh_attn_plan_create_ring(w.S, w.P, w.causal) if args.plan == "ring"
+     else m.mesh_attn_plan_create(w.S, w.P, w.causal, w.kvr, w.greedy))
+    plan_ms = (time.perf_counter() - t_plan) * 1e3
     po, pl = m.new_partials(plan, w.B, w.Hq, w.d, dev)
     wsp = m.new_workspace(plan, dev, qd, kd)
     st = m.new_status(dev)
@@ -482,7 +487,7 @@ def main():
         "roofline": roof,
         "merge": {"bound": "hbm", "achieved": merge_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                   "frac": merge_gbs / peaks["hbm_gbs"], "bytes_per_launch": mbytes, "ms": merge_ms},
-        "tile_fwd_ms": tile_ms, "merge_ms": merge_ms, "backward": bwd,
+        "tile_fwd_ms": tile_ms, "merge_ms": merge_ms, "plan_ms": plan_ms, "backward": bwd,
         "comm_counted": counted_volumes(m, w),
         "cpu_baseline": cpu_base, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
