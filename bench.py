@@ -326,6 +326,8 @@ def run_backward(m, w, plan, qd, kd, vd, O, LSE, dev, args, stream, flops):
         line["roofline"] = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                             "frac": tflops / peaks["bf16_tflops"], "traffic": None,
                             "kernel": "bwd_dkdv_kernel + bwd_dq_kernel"}
+        if peaks.get("bf16_tflops_sustained"):
+            line["roofline"]["frac_of_sustained"] = tflops / peaks["bf16_tflops_sustained"]
     return line
 
 
@@ -469,6 +471,8 @@ def main():
         roof = {"bound": "tensor", "achieved": tile_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": tile_tflops / peaks["bf16_tflops"], "traffic": traffic,
                 "kernel": "tile_fwd_tc_kernel", "peak_kind": f"{peak_kind} bf16 dense burst"}
+        if peaks.get("bf16_tflops_sustained"):  # context: the power-capped, seconds-long GEMM rate
+            roof["frac_of_sustained"] = tile_tflops / peaks["bf16_tflops_sustained"]
         launches_per_step = 2  # tile, merge
     else:
         # fp32 inputs: every product is six bf16 tensor-core products of the operands' exact
