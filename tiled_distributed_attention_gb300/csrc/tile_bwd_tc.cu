@@ -31,11 +31,13 @@
 //   so the exponentials of block i+1 overlap dK(i) and dP^T(i+1), and dS^T(i+1) overlaps
 //   dV(i+1) and S^T(i+2).  LSE and D of the block's query columns are broadcast from shared
 //   memory.
-// dq (unit = forward work item, batch, head, 128-row block): Q and dO stay in shared memory; K
-//   and V blocks of the item's KV partitions stream through three and two stages.
-//   TMEM: S(even) | S(odd) | dP | dQ: S(j+2) is issued as soon as its K block has landed, so
-//   the exponentials of block j+1 run while dQ(j) and dP(j+1) execute.  LSE and D of a row are
-//   thread-local.
+// dq (unit = forward work item, batch, head, 128-row block): Q and dO are copied once per unit
+//   from shared memory into TMEM by the epilogue warps and feed S = Q K^T and dP = dO V^T as
+//   A operands from TMEM, so those products read only the streamed K or V block from shared
+//   memory; K and V blocks of the item's KV partitions stream through three and two stages.
+//   TMEM: S | dP | dQ | Q | dO (bf16).  S(j+1) is issued as soon as the elementwise warps have
+//   read S(j) into registers, so it computes while they exponentiate block j; LSE and D of a
+//   row are thread-local.
 // Every mbarrier wait is bounded; a timeout records MESH_ATTN_ERR_DEVICE_TIMEOUT, the CTA stops,
 // drains its copies and products and frees its tensor memory.
 #include <cuda.h>
@@ -110,7 +112,7 @@ struct Layout {
                        B_S = B_BE + NSB, B_DP = B_S + 2, B_P = B_DP + 1, B_DS = B_P + 1, B_ACC = B_DS + 1,
                        B_DRAIN = B_ACC + 1, B_VEC = B_DRAIN + 1, B_RESE = B_VEC + 2, B_ACCE = B_RESE + 1,
                        B_UF = B_ACCE + 1, B_UE = B_UF + 2, B_ACC2 = B_UE + 2, B_ACCE2 = B_ACC2 + 1,
-                       NBARS = B_ACCE2 + 1;
+                       B_SREAD = B_ACCE2 + 1, B_QTF = B_SREAD + 1, B_QTE = B_QTF + 1, NBARS = B_QTE + 1;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag
   static constexpr uint32_t RING_OFF = MISC_OFF + 16;         // unit ring: 2 decoded units, 16 ints each
   static constexpr uint32_t TOTAL = RING_OFF + 2 * 64;
@@ -856,7 +858,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Ly::B_RES), 1);
-    mbar_init(bar(Ly::B_RESE), 1);
+    mbar_init(bar(Ly::B_RESE), N_EPI);  // the epilogue warps have copied Q and dO into TMEM
     for (int s = 0; s < Ly::NSA; ++s) {
       mbar_init(bar(Ly::B_AF + s), 1);
       mbar_init(bar(Ly::B_AE + s), 1);
@@ -866,7 +868,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(Ly::B_BE + s), 1);
     }
     mbar_init(bar(Ly::B_S), 1);
-    mbar_init(bar(Ly::B_S + 1), 1);
+    mbar_init(bar(Ly::B_SREAD), N_EW);  // S has been loaded by every elementwise warp
+    mbar_init(bar(Ly::B_QTF), N_EPI);   // Q and dO of the unit are in TMEM
+    mbar_init(bar(Ly::B_QTE), 1);       // the unit's last S and dP products are done with them
     mbar_init(bar(Ly::B_DP), 1);
     mbar_init(bar(Ly::B_DS), N_EW);  // one lane of each elementwise warp
     mbar_init(bar(Ly::B_ACC), 1);
@@ -924,7 +928,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int row = wq * 32 + lane;           // TMEM lane = query row within the block
     const int c_base = hf * 64;               // this warp's key columns [c_base, c_base + 64)
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const uint32_t tm_dp = tmem + lane_base + 256u;  // dP, then dS (bf16)
+    const uint32_t tm_s = tmem + lane_base;          // S
+    const uint32_t tm_dp = tmem + lane_base + 128u;  // dP, then dS (bf16)
     bool ok = run;
     int v = -1;
     DqUnit x;
@@ -963,9 +968,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (prm.causal && kp == p && kbk == qb) hi = min(hi, row + 1);  // diagonal block
         hi -= c_base;                                                   // in this half's columns
         const bool any_mask = __any_sync(0xffffffffu, hi < 64);
-        const uint32_t tm_s = tmem + lane_base + (uint32_t)((g & 1) * 128);
-        ok = mbar_wait(bar(Ly::B_S + (int)(g & 1)), (uint32_t)((g >> 1) & 1), prm.wait_limit_ns, abort_flag,
-                       prm.status, ROLE_EW, j);
+        ok = mbar_wait(bar(Ly::B_S), (uint32_t)(g & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW, j);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
@@ -973,6 +976,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_ld32(tm_s + (uint32_t)c_base, pv);
         tmem_ld32(tm_s + (uint32_t)c_base + 32u, pv + 32);
         tc_wait_ld();
+        // S(g) is in registers: the next block's S may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(Ly::B_SREAD));
         if (any_mask) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
@@ -1026,28 +1033,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     regs_dec<MMA_REGS>();
     if (warp == WARP_MMA) {
     // ================================================================ MMA issuer
-    constexpr uint32_t idesc_ss = idesc_bf16_f32(BM, BM, false);  // S = Q K^T, dP = dO V^T
+    constexpr uint32_t idesc_sk = idesc_bf16_f32(BM, BM, false);  // S = Q K^T, dP = dO V^T: K-major B
     constexpr uint32_t idesc_ts = idesc_bf16_f32(BM, D, true);    // dQ += dS K, K MN-major
-    const uint64_t qdesc = smem_desc_sw128(sb + Ly::RES0, 16u, 1024u);
-    const uint64_t gdesc = smem_desc_sw128(sb + Ly::RES1, 16u, 1024u);
+    const uint32_t tm_qt = tmem + 384u, tm_gt = tmem + 384u + (uint32_t)(D / 2);  // Q and dO (bf16)
     constexpr uint64_t TILE16 = Ly::TILE >> 4;
     const uint64_t a_kmaj = smem_desc_sw128(sb + Ly::A0, 16u, 1024u);  // K stages
     const uint64_t a_mn = smem_desc_sw128(sb + Ly::A0, Ly::BOX, 1024u);
     const uint64_t b_kmaj = smem_desc_sw128(sb + Ly::B0, 16u, 1024u);  // V stages
-    auto issue_s = [&](int64_t g) {  // S(g) = Q K(g)^T into S buffer g & 1
+    // Q and dO come from TMEM (copied there once per unit), so these products read only the
+    // streamed K or V block from shared memory
+    auto issue_s = [&](int64_t g) {  // S(g) = Q K(g)^T
       const uint64_t kd = a_kmaj + (uint64_t)(g % Ly::NSA) * TILE16;
-      const uint32_t buf = (uint32_t)(g & 1);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        tc_mma_ss_warp(tmem + buf * 128u, qdesc + kmaj_off<D>(kk), kd + kmaj_off<D>(kk), idesc_ss, kk > 0);
-      tc_commit_warp(bar(Ly::B_S + (int)buf));
+        tc_mma_ts_warp(tmem, tm_qt + (uint32_t)(kk * 8), kd + kmaj_off<D>(kk), idesc_sk, kk > 0 ? 1u : 0u);
+      tc_commit_warp(bar(Ly::B_S));
     };
     auto issue_dp = [&](int64_t g) {  // dP(g) = dO V(g)^T; V(g) is read by this product only
       const int sbb = (int)(g % Ly::NSB);
       const uint64_t vd = b_kmaj + (uint64_t)sbb * TILE16;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        tc_mma_ss_warp(tmem + 256u, gdesc + kmaj_off<D>(kk), vd + kmaj_off<D>(kk), idesc_ss, kk > 0);
+        tc_mma_ts_warp(tmem + 128u, tm_gt + (uint32_t)(kk * 8), vd + kmaj_off<D>(kk), idesc_sk, kk > 0 ? 1u : 0u);
       tc_commit_warp(bar(Ly::B_DP));
       tc_commit_warp(bar(Ly::B_BE + sbb));
     };
@@ -1055,7 +1062,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t kd = a_mn + (uint64_t)(g % Ly::NSA) * TILE16;
 #pragma unroll
       for (int kk = 0; kk < BM / 16; ++kk)
-        tc_mma_ts_warp(tmem + 384u, tmem + 256u + packed_col(kk), kd + (uint64_t)(kk * 128), idesc_ts,
+        tc_mma_ts_warp(tmem + 256u, tmem + 128u + packed_col(kk), kd + (uint64_t)(kk * 128), idesc_ts,
                        (!first || kk > 0) ? 1u : 0u);
       tc_commit_warp(bar(Ly::B_AE + (int)(g % Ly::NSA)));  // K(g): read by S(g) and dQ(g)
     };
@@ -1067,26 +1074,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       return mbar_wait_warp(bar(Ly::B_BF + (int)(g % Ly::NSB)), (uint32_t)((g / Ly::NSB) & 1), prm.wait_limit_ns,
                             abort_flag, prm.status, ROLE_MMA, (int32_t)g);
     };
-    int nres = 0;
-    // S(0), dP(0) and S(1) of a unit whose first block is g: issued as soon as its resident Q and
-    // dO have landed (for every unit but the first, after the previous unit's last dQ)
+    int nqt = 0;
+    // S(0) and dP(0) of a unit whose first block is g: issued as soon as its Q and dO are in TMEM
+    // (for every unit but the first, after the previous unit's last dQ)
     auto start_unit = [&](const DqUnit& y, int64_t g) -> bool {
-      if (!mbar_wait_warp(bar(Ly::B_RES), (uint32_t)(nres & 1), prm.wait_limit_ns, abort_flag, prm.status,
+      if (!mbar_wait_warp(bar(Ly::B_QTF), (uint32_t)(nqt & 1), prm.wait_limit_ns, abort_flag, prm.status,
                           ROLE_MMA, -1))
         return false;
-      ++nres;
+      ++nqt;
       if (!wait_a(g)) return false;
       tc_fence_after();
       issue_s(g);
       if (!wait_b(g)) return false;
       tc_fence_after();
       issue_dp(g);
-      if (y.NB == 1) tc_commit_warp(bar(Ly::B_RESE));  // the unit's last S and dP are issued
-      if (y.NB > 1) {
-        if (!wait_a(g + 1)) return false;
-        tc_fence_after();
-        issue_s(g + 1);
-      }
+      if (y.NB == 1) tc_commit_warp(bar(Ly::B_QTE));  // the unit's last S and dP are issued
       return true;
     };
     bool ok = run;
@@ -1107,10 +1109,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int NB = x.NB;
       for (int j = 0; j < NB && ok; ++j) {
         const int64_t g = g0 + j;
-        // dS(g) is in TMEM, and S(g) has been read, so its buffer is free for S(g+2).  (One barrier per
-        // block, passed in order: a second "S read" barrier could complete for block g+1, whose S is
-        // issued two blocks ahead, before this warp observed block g -- two phases ahead of its
-        // parity wait.)
+        // S(g) has been read into registers: S(g+1) may overwrite it.  (The next block's S is
+        // issued only after this wait, so the barrier cannot run a phase ahead of it.)
+        if (j + 1 < NB) {
+          ok = mbar_wait_warp(bar(Ly::B_SREAD), (uint32_t)(g & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                              ROLE_MMA, j);
+          if (!ok) break;
+          ok = wait_a(g + 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(g + 1);
+        }
         ok = mbar_wait_warp(bar(Ly::B_DS), (uint32_t)(g & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
         if (!ok) break;
         if (j == 0 && k_unit > 0) {  // the previous unit's dQ has been copied out of TMEM
@@ -1126,13 +1135,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!ok) break;
           tc_fence_after();
           issue_dp(g + 1);
-          if (j + 2 == NB) tc_commit_warp(bar(Ly::B_RESE));  // the unit's last S and dP are issued
-        }
-        if (j + 2 < NB) {
-          ok = wait_a(g + 2);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(g + 2);
+          if (j + 2 == NB) tc_commit_warp(bar(Ly::B_QTE));  // the unit's last S and dP are issued
         }
       }
       if (!ok) break;
@@ -1257,20 +1260,72 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ================================================================ epilogue
-    // Drains each unit's dQ while the other roles run the next one, releasing it (so the next
-    // unit may overwrite it) once its last TMEM load has completed.
+    // Per unit: copy its resident Q and dO from shared memory into TMEM (as the A operands of S
+    // and dP) as soon as the previous unit's last S and dP products are done with the TMEM copy,
+    // releasing the shared buffers to the producer; then drain the previous unit's dQ while the
+    // other roles run this one, releasing it (so the next unit may overwrite it) once its last
+    // TMEM load has completed.
     regs_dec<EPI_REGS>();
     const int wq = warp & 3;  // TMEM lane quadrant
-    const uint32_t tm_dq = tmem + ((uint32_t)(wq * 32) << 16) + 384u;
+    const int r = wq * 32 + lane;  // this thread's row of the 128-row block
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t tm_dq = tmem + lane_base + 256u;
+    const uint32_t tm_qt = tmem + lane_base + 384u, tm_gt = tm_qt + (uint32_t)(D / 2);
     bool ok = run;
-    int v = -1, k_unit = 0;
+    int v = -1, k_unit = 0, ncopy = 0;
     DqUnit x;
+    // row r of a 128 x D bf16 block landed by TMA in 64-column boxes with 128-byte swizzle (the
+    // 16-byte chunk j of a 128-byte row sits at chunk j ^ (r mod 8)), packed two columns per TMEM
+    // column from column `dst`
+    auto copy_row = [&](uint32_t src_off, uint32_t dst) {
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        const uint8_t* rowp = smem + src_off + (uint32_t)c * Ly::BOX + (uint32_t)r * 128u;
+        uint32_t w[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 q = *reinterpret_cast<const uint4*>(rowp + ((j ^ (r & 7)) << 4));
+          w[4 * j] = q.x, w[4 * j + 1] = q.y, w[4 * j + 2] = q.z, w[4 * j + 3] = q.w;
+        }
+        tmem_st32(dst + (uint32_t)(32 * c), w);
+      }
+    };
+    auto copy_in = [&]() -> bool {
+      if (!mbar_wait_warp(bar(Ly::B_RES), (uint32_t)(ncopy & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                          ROLE_EPI, -1))
+        return false;
+      if (ncopy > 0 && !mbar_wait_warp(bar(Ly::B_QTE), (uint32_t)((ncopy - 1) & 1), prm.wait_limit_ns, abort_flag,
+                                       prm.status, ROLE_EPI, -1))
+        return false;
+      tc_fence_after();
+      copy_row(Ly::RES0, tm_qt);
+      copy_row(Ly::RES1, tm_gt);
+      tc_wait_st();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // reads done before the next TMA write
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(Ly::B_QTF));
+        mbar_arrive(bar(Ly::B_RESE));
+      }
+      ++ncopy;
+      return true;
+    };
     if (ok) ok = take(v, x, ROLE_EPI);
+    if (ok && v >= 0 && x.ok && x.NB >= 1) ok = copy_in();
     while (ok && v >= 0) {
       if (!x.ok || x.NB < 1) {
         bad_unit(v, ROLE_EPI);
         ok = false;
         break;
+      }
+      int vn = -1;
+      DqUnit xn;
+      ok = take(vn, xn, ROLE_EPI);
+      if (!ok) break;
+      if (vn >= 0 && xn.ok && xn.NB >= 1) {
+        ok = copy_in();
+        if (!ok) break;
       }
       const int64_t row0 =
           (((int64_t)x.b * prm.Hq + x.h) * prm.n_slots + x.it.slot) * L + (int64_t)x.qb * BM + wq * 32;
@@ -1292,7 +1347,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         store_rows<D>(t, prm.scale, prm.dq_part, row0, rows_valid, c, lane);
       }
       ++k_unit;
-      ok = take(v, x, ROLE_EPI);
+      v = vn;
+      x = xn;
     }
   }
 
