@@ -93,9 +93,10 @@ struct Params {
   int64_t wait_limit_ns;
 };
 
-// Shared memory: the resident pair (K, V in dkdv; Q, dO in dq), NSA stages of stream A (the
-// operand of the S product, needed two blocks ahead: Q in dkdv, K in dq) and NSB stages of
-// stream B (dO in dkdv, V in dq).  224 KB for d = 128 leaves no room to align the base by hand:
+// Shared memory: the resident pair (K, V in dkdv; in dq the landing buffers of Q and dO, which
+// the epilogue warps copy into TMEM), NSA stages of stream A (the operand of the S product, which
+// the next block's S needs while the current block's dK or dQ still reads it: Q in dkdv, K in
+// dq) and NSB stages of stream B (dO in dkdv, V in dq).  224 KB for d = 128 leaves no room to align the base by hand:
 // the kernels check that the dynamic shared window starts 1024-aligned (it does on sm_100-class
 // parts, whose window starts at a 1 KB-aligned offset) and report MESH_ATTN_ERR_INTERNAL if not.
 template <int D>
