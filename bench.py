@@ -36,6 +36,24 @@ def algorithmic_flops(w) -> float:
     return 4.0 * w.d * w.B * w.Hq * pairs
 
 
+def executed_flops_fwd(m, plan, w) -> float:
+    """Flops the bf16 tile kernel's products execute: full 128 x 128 blocks, including the masked
+    half of causal diagonal blocks and the padding of a ragged last block (a diagnostic beside
+    the algorithmic count).  A unit is a pair of 128-row query tiles of one work item, and it
+    visits every 128-key block of the item's KV partitions up to its last tile on the causal
+    diagonal partition."""
+    items, _, kvs = m.mesh_attn_plan_order(plan)
+    nb = -(-w.L // 128)
+    per_item = 0
+    for (p, _t, _slot), kl in zip(items, kvs):
+        for a0 in range(0, nb, 2):
+            ntiles = min(2, nb - a0)
+            a_max = a0 + ntiles - 1
+            blocks = sum(min(nb, a_max + 1) if (w.causal and k == p) else nb for k in kl)
+            per_item += blocks * ntiles
+    return 4.0 * 128 * 128 * w.d * per_item * w.B * w.Hq
+
+
 def sample_flops(w, rows: np.ndarray) -> float:
     vis = (rows + 1).sum() if w.causal else rows.size * w.S
     return 4.0 * w.d * float(vis)
@@ -473,6 +491,9 @@ def main():
                 "kernel": "tile_fwd_tc_kernel", "peak_kind": f"{peak_kind} bf16 dense burst"}
         if peaks.get("bf16_tflops_sustained"):  # context: the power-capped, seconds-long GEMM rate
             roof["frac_of_sustained"] = tile_tflops / peaks["bf16_tflops_sustained"]
+        exe = executed_flops_fwd(m, plan, w)
+        roof["executed_tflops"] = exe / (tile_ms * 1e-3) / 1e12  # full blocks, masked halves included
+        roof["executed_over_algorithmic"] = exe / flops
         launches_per_step = 2  # tile, merge
     else:
         # fp32 inputs: every product is six bf16 tensor-core products of the operands' exact
