@@ -15,11 +15,14 @@
 //               elected lane of the converged warp; completion by tcgen05.commit
 //   warp 9      producer: TMA loads of 128 x 64 bf16 boxes with 128-byte swizzle
 //   warps 10-11 idle
-//   warps 12-15 epilogue: one per TMEM lane quadrant; copies a unit's accumulators out of TMEM
-//               and stores its partial rows while the other roles run the next unit
+//   warps 12-15 (dq only) epilogue: one per TMEM lane quadrant; copies each unit's Q and dO into
+//               TMEM, and drains the unit's dQ accumulator and stores its partial rows while the
+//               other roles run the next unit.  In dkdv the elementwise warps drain dV and dK at
+//               the unit boundary instead: drained during the next unit, the TMEM reads of the
+//               two accumulators slowed that unit's products down.
 // Across units: the next unit's resident block loads as soon as the last products reading the
 // current one have completed, its first products are issued right after the current unit's
-// last accumulation, and an accumulator is overwritten only after the epilogue has copied it.
+// last accumulation, and an accumulator is overwritten only after it has been copied out.
 //
 // dkdv (unit = KV slot, batch, KV head, 128-key block): K and V stay in shared memory; Q and dO
 // blocks of the slot's query rows (over the KV head's query heads) stream through three and two
@@ -311,15 +314,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar(Ly::B_P), N_EW);  // one lane of each elementwise warp
     mbar_init(bar(Ly::B_DS), N_EW);
     mbar_init(bar(Ly::B_ACC), 1);
-    mbar_init(bar(Ly::B_ACCE), N_EPI);  // one lane of each epilogue warp
+    mbar_init(bar(Ly::B_ACCE), N_EW);  // one lane of each elementwise warp
     mbar_init(bar(Ly::B_ACC2), 1);
-    mbar_init(bar(Ly::B_ACCE2), N_EPI);
+    mbar_init(bar(Ly::B_ACCE2), N_EW);
     mbar_init(bar(Ly::B_DRAIN), 1);
     mbar_init(bar(Ly::B_VEC), BM);  // every elementwise thread has written its LSE / D value
     mbar_init(bar(Ly::B_VEC + 1), BM);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(Ly::B_UF + s), 1);
-      mbar_init(bar(Ly::B_UE + s), N_EW + 1 + N_EPI);  // elementwise, MMA and epilogue warps read a unit
+      mbar_init(bar(Ly::B_UE + s), N_EW + 1);  // the elementwise warps and the MMA warp read a unit
     }
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0) ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -399,6 +402,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     int64_t g0 = 0;  // global index of the unit's first query block
+    int k_unit = 0;
     while (ok && v >= 0) {
       if (!x.ok || x.NBQ < 1) {
         bad_unit(v, ROLE_EW);
@@ -493,7 +497,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) mbar_arrive(bar(Ly::B_DS));
       }
       if (!ok) break;
-      // the next unit, and its first block's LSE and D (the epilogue warps drain this one)
+      // the next unit, and its first block's LSE and D, before this unit's epilogue
       int vn = -1;
       KvUnit xn;
       ok = take(vn, xn, ROLE_EW);
@@ -504,6 +508,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (hf == 0) fetch(xn, cur);
         }
       }
+      // ---- epilogue: this half's columns of the dV and dK rows of this key block.  It runs here,
+      // at the unit boundary where the tensor pipe has little else to do: drained by separate
+      // warps during the next unit, the TMEM reads slowed that unit's products down.
+      ok = mbar_wait(bar(Ly::B_ACC2), (uint32_t)(k_unit & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_EW,
+                     -1);  // dK's last product, and so dV's, has completed
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      {
+        const uint32_t tm_dv = tmem + lane_base + 256u + (uint32_t)(hf * (D / 2));
+        const uint32_t tm_dk = tm_dv + (uint32_t)D;
+        const int64_t row0 =
+            (((int64_t)x.b * prm.Hkv + x.hk) * prm.n_kv_slots + x.it.slot) * L + (int64_t)kb * BM + wq * 32;
+        const int rows_valid = (int)max((int64_t)0, min((int64_t)32, L - ((int64_t)kb * BM + wq * 32)));
+        float acc[D / 2];
+#pragma unroll
+        for (int c = 0; c < D / 2; c += 32) tmem_ld32(tm_dv + (uint32_t)c, acc + c);
+        tc_wait_ld();
+#pragma unroll
+        for (int c = 0; c < D / 2; c += 32)
+          store_rows<D>(*reinterpret_cast<const float(*)[32]>(acc + c), 1.f, prm.dv_part, row0, rows_valid,
+                        hf * (D / 2) + c, lane);
+#pragma unroll
+        for (int c = 0; c < D / 2; c += 32) tmem_ld32(tm_dk + (uint32_t)c, acc + c);
+        tc_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {  // both accumulators are copied out: the next unit may overwrite them
+          mbar_arrive(bar(Ly::B_ACCE));
+          mbar_arrive(bar(Ly::B_ACCE2));
+        }
+#pragma unroll
+        for (int c = 0; c < D / 2; c += 32)
+          store_rows<D>(*reinterpret_cast<const float(*)[32]>(acc + c), prm.scale, prm.dk_part, row0, rows_valid,
+                        hf * (D / 2) + c, lane);
+      }
+      ++k_unit;
       g0 += NBQ;
       v = vn;
       x = xn;
@@ -743,53 +784,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_drain(bar(Ly::B_BF + (int)(j % Ly::NSB)), (uint32_t)((j / Ly::NSB) & 1), DRAIN_NS);
     }
   } else {
-    // ================================================================ epilogue
-    // Drains the accumulators of each unit while the other roles run the next one: dV as soon
-    // as its last product completes, then dK; each is released (so the next unit may overwrite
-    // it) once its last TMEM load has completed, before the stores of that chunk.
+    // warps 12-15 have no role in this kernel (the elementwise warps drain the accumulators)
     regs_dec<EPI_REGS>();
-    const int wq = warp & 3;  // TMEM lane quadrant
-    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const uint32_t tm_dv = tmem + lane_base + 256u;
-    const uint32_t tm_dk = tmem + lane_base + 256u + (uint32_t)D;
-    bool ok = run;
-    int v = -1, k_unit = 0;
-    KvUnit x;
-    if (ok) ok = take(v, x, ROLE_EPI);
-    while (ok && v >= 0) {
-      if (!x.ok || x.NBQ < 1) {
-        bad_unit(v, ROLE_EPI);
-        ok = false;
-        break;
-      }
-      const int64_t row0 =
-          (((int64_t)x.b * prm.Hkv + x.hk) * prm.n_kv_slots + x.it.slot) * L + (int64_t)x.kb * BM + wq * 32;
-      const int rows_valid = (int)max((int64_t)0, min((int64_t)32, L - ((int64_t)x.kb * BM + wq * 32)));
-      for (int which = 0; which < 2 && ok; ++which) {
-        ok = mbar_wait_warp(bar(which ? Ly::B_ACC2 : Ly::B_ACC), (uint32_t)(k_unit & 1), prm.wait_limit_ns, abort_flag,
-                            prm.status, ROLE_EPI, -1);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t tm = which ? tm_dk : tm_dv;
-        float* dst = which ? prm.dk_part : prm.dv_part;
-        const float mul = which ? prm.scale : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          float t[32];
-          tmem_ld32(tm + (uint32_t)c, t);
-          tc_wait_ld();
-          if (c + 32 == D) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(which ? Ly::B_ACCE2 : Ly::B_ACCE));
-          }
-          store_rows<D>(t, mul, dst, row0, rows_valid, c, lane);
-        }
-      }
-      if (!ok) break;
-      ++k_unit;
-      ok = take(v, x, ROLE_EPI);
-    }
   }
 
   tc_fence_before();
