@@ -9,6 +9,7 @@
 // A streaming HBM-bound kernel.  One CTA of 256 threads owns ROWS consecutive rows of one
 // (batch, head, partition); because the slots of a partition hold the same rows at a stride of
 // L rows, the CTA's share of each slot is one contiguous block of ROWS * d floats (16 KB).
+//   0. the loads of the first two slots' blocks go out first (they do not need the weights);
 //   1. the CTA reads its ROWS x n_slots LSE values (coalesced per slot) into shared memory;
 //   2. one warp turns them into per-row weights exp(lse_t - lse) and writes the row LSE;
 //   3. every thread streams 16-byte pieces of each slot's contiguous block (consecutive
@@ -67,6 +68,20 @@ __global__ void __launch_bounds__(THREADS) merge_kernel(const MergeArgs a, int n
     return;
   }
   const int64_t row_base = ((int64_t)bh * a.n_slots + s0) * L + r0;  // slot s0, row r0
+  const float4* src = reinterpret_cast<const float4*>(a.part_o + row_base * D);
+  const int64_t slot_stride = (int64_t)L * V4_PER_ROW;  // float4 per slot
+
+  // 0. the first two slots' blocks do not depend on the weights: their loads go out first and
+  //    land while the LSEs are read and the weights computed
+  float4 v[2][PER_THREAD];
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int k = 0; k < PER_THREAD; ++k) {
+      const int idx = tid + k * THREADS;
+      v[q][k] = (q < ns && idx / V4_PER_ROW < nrows) ? __ldcs(src + q * slot_stride + idx)
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 
   // 1. slot LSEs of the CTA's rows
   for (int i = tid; i < ns * ROWS; i += THREADS) {
@@ -91,15 +106,24 @@ __global__ void __launch_bounds__(THREADS) merge_kernel(const MergeArgs a, int n
     if (r < nrows) a.LSE[(int64_t)bh * a.S + (int64_t)p * L + r0 + r] = (W > 0.f) ? Ms + logf(W) : -INFINITY;
   }
   __syncthreads();
-  // 3. stream each slot's contiguous block
-  const float4* src = reinterpret_cast<const float4*>(a.part_o + row_base * D);
-  const int64_t slot_stride = (int64_t)L * V4_PER_ROW;  // float4 per slot
+  // 3. stream each slot's contiguous block (slots 0 and 1 are already in registers)
   float4 acc[PER_THREAD];
 #pragma unroll
   for (int k = 0; k < PER_THREAD; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  int t = 0;
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+    if (q < ns) {
+#pragma unroll
+      for (int k = 0; k < PER_THREAD; ++k) {
+        const float w = w_s[q][(tid + k * THREADS) / V4_PER_ROW];
+        acc[k].x = fmaf(w, v[q][k].x, acc[k].x);
+        acc[k].y = fmaf(w, v[q][k].y, acc[k].y);
+        acc[k].z = fmaf(w, v[q][k].z, acc[k].z);
+        acc[k].w = fmaf(w, v[q][k].w, acc[k].w);
+      }
+    }
+  int t = 2;
   for (; t + 2 <= ns; t += 2) {
-    float4 v[2][PER_THREAD];
 #pragma unroll
     for (int q = 0; q < 2; ++q)
 #pragma unroll
