@@ -1,9 +1,11 @@
 """Benchmark of the Mesh-Attention hot path on GB300: one step = tile forward over every
 (Q partition, tile) item of the plan + LSE merge, on a synthetic workload resident in HBM.
 
-Prints one JSON line (rank 0).  Default workload: bf16 causal, B=1, Hq=Hkv=16, S=16384,
-d=128, P=16 partitions of 1024 tokens on a 4x4 mesh with KV Partition Rotation and greedy
-order.  `--impl reference` times the fp64 CPU oracle on the host cores instead.
+Prints one JSON line (rank 0).  Default workload: the largest single-GPU configuration, the
+merge-heavy long-context stress case: bf16 causal, B=1, Hq=16, Hkv=4, S=262144, d=128, K rows
+scaled by 4, P=1024 partitions of 256 tokens on a 32x32 mesh with KV Partition Rotation and
+greedy order (68 GB of fp32 partials).  The backward pass is measured beside it on the bf16
+causal 16K workload.  `--impl reference` times the fp64 CPU oracle on the host cores instead.
 """
 from __future__ import annotations
 
@@ -57,6 +59,36 @@ def executed_flops_fwd(m, plan, w) -> float:
 def sample_flops(w, rows: np.ndarray) -> float:
     vis = (rows + 1).sum() if w.causal else rows.size * w.S
     return 4.0 * w.d * float(vis)
+
+
+def rows_for_budget(w, flops_budget: float) -> int:
+    """Seeded rows per head whose oracle work (4 d per visible pair, every head) is about
+    flops_budget: a bounded sample of the workload for the CPU timing."""
+    avg_vis = (w.S + 1) / 2 if w.causal else w.S
+    n = int(flops_budget / (4.0 * w.d * avg_vis * w.Hq * w.B))
+    return max(16, min(w.S, 4096, n))
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                val = line.split(":", 1)[1].strip()
+                if val and not val.isdigit():
+                    return val
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
 
 
 def merge_bytes(w, n_slots: int) -> float:
@@ -157,21 +189,24 @@ def dist_env():
 _INPUTS = {}
 
 
-def time_oracle(w, n_rows: int, heads, threads: int):
-    """fp64 oracle on n_rows seeded rows of the given heads; returns (seconds, algorithmic flops)."""
+def time_oracle(w, n_rows: int, heads, threads: int, qkv=None):
+    """fp64 oracle on n_rows seeded rows of the given heads (batch 0); returns (seconds, algorithmic
+    flops, {head: (rows, O, LSE)})."""
     from oracle.attention import attention_rows, default_scale
     torch.set_num_threads(threads)
     if (w.name, n_rows) not in _INPUTS:
-        _INPUTS[(w.name, n_rows)] = (make_qkv(w), sample_rows(w, n_rows))
+        _INPUTS[(w.name, n_rows)] = (qkv if qkv is not None else make_qkv(w), sample_rows(w, n_rows))
     (q, k, v), rows = _INPUTS[(w.name, n_rows)]
     g = w.Hq // w.Hkv
     t0 = time.perf_counter()
     fl = 0.0
+    out = {}
     for h in heads:
         pos = torch.as_tensor(rows[0, h])
-        attention_rows(q[0, h].double()[pos], pos, k[0, h // g], v[0, h // g], default_scale(w.d), w.causal)
+        o, lse = attention_rows(q[0, h].double()[pos], pos, k[0, h // g], v[0, h // g], default_scale(w.d), w.causal)
         fl += sample_flops(w, rows[0, h])
-    return time.perf_counter() - t0, fl
+        out[h] = (rows[0, h], o, lse)
+    return time.perf_counter() - t0, fl, out
 
 
 def run_reference(args, w):
@@ -179,12 +214,14 @@ def run_reference(args, w):
     if rank != 0:
         return
     threads = os.cpu_count() or 1
-    rows_per_step = 256
+    # about 1.5e10 oracle flops (well under a second of host time) per step, at most 256 rows
+    avg_vis = (w.S + 1) / 2 if w.causal else w.S
+    rows_per_step = max(16, min(256, int(1.5e10 / (4.0 * w.d * avg_vis))))
     for i in range(args.warmup):
         time_oracle(w, rows_per_step, [i % w.Hq], threads)
     secs, fl = 0.0, 0.0
     for i in range(args.steps):
-        s, f = time_oracle(w, rows_per_step, [i % w.Hq], threads)
+        s, f, _ = time_oracle(w, rows_per_step, [i % w.Hq], threads)
         secs += s
         fl += f
     value = fl / secs / 1e12
@@ -193,7 +230,8 @@ def run_reference(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(w),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+                             "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -289,13 +327,20 @@ def run_e2e(m, w, args, q, k, v, dev, flops, world, barrier):
             "serial_value": job_throughput(world, flops, s_ms), "serial_ms_per_step": s_ms}
 
 
-def run_backward(m, w, plan, qd, kd, vd, O, LSE, dev, args, stream, flops):
-    """Time the backward pass (D = dO . O, tile backward, reduce) with CUDA events, inputs resident.
+def run_backward(m, w, dev, args, stream):
+    """Time the backward pass (D = dO . O, tile backward, reduce) with CUDA events, inputs resident,
+    on workload w (its own inputs; the forward's O and LSE come from one untimed forward call).
 
     Algorithmic flops of the tile backward: the four gradient products dP = dO V^T, dV = P^T dO,
     dQ = dS K, dK = dS^T Q over the visible pairs = 2x the forward's; the kernels also recompute
     S (dK/dV kernel) and S, dP (dQ kernel): executed = 3.5x the forward's.
     """
+    flops = algorithmic_flops(w)
+    q, k, v = make_qkv(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    del q, k, v
+    plan = m.mesh_attn_plan_create(w.S, w.P, w.causal, w.kvr, w.greedy)
+    O, LSE = m.mesh_attention(qd, kd, vd, w.P, w.causal, plan=plan)
     dO = make_do(w).to(dev)
     dq_p, dk_p, dv_p = m.new_bwd_partials(plan, w.B, w.Hq, w.Hkv, w.d, dev)
     wsb = m.new_bwd_workspace(plan, dev)
@@ -335,7 +380,7 @@ def run_backward(m, w, plan, qd, kd, vd, O, LSE, dev, args, stream, flops):
     nq, nkv = m.mesh_attn_bwd_partials_size(plan, w.B, w.Hq, w.Hkv, w.d)
     red_bytes = 4.0 * (nq + 2 * nkv) + es * (w.B * w.Hq * w.S * w.d + 2 * w.B * w.Hkv * w.S * w.d)
     prep_bytes = 2.0 * es * w.B * w.Hq * w.S * w.d + 4.0 * w.B * w.Hq * w.S
-    line = {"ms_per_step": prep_ms + tile_ms + red_ms, "steps": steps,
+    line = {"workload": w.name, "ms_per_step": prep_ms + tile_ms + red_ms, "steps": steps,
             "tile_bwd_ms": tile_ms, "prep_ms": prep_ms, "reduce_ms": red_ms,
             "flops_per_step": alg, "tflops": tflops, "unit": "TFLOP/s",
             "executed_tflops": 3.5 * flops / (tile_ms * 1e-3) / 1e12,
@@ -358,10 +403,12 @@ def workload_config(w, plan="mesh"):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="bf16_causal_16k", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="stress_256k", choices=sorted(WORKLOADS))
+    ap.add_argument("--backward-workload", default="bf16_causal_16k", choices=sorted(WORKLOADS),
+                    help="workload of the backward-pass object of the line")
     ap.add_argument("--plan", default="mesh", choices=["mesh", "ring"],
                     help="tile assignment: sqrt(P) x sqrt(P) mesh with KVR (default) or Ring-Attention rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -391,15 +438,26 @@ def main():
             import torch.distributed as dist
             dist.barrier()
 
-    # cpu baseline first (before any GPU work is queued), rank 0 at N=1 only
-    cpu_base = None
+    q, k, v = make_qkv(w)
+
+    # cpu baseline first (before any GPU work is queued), rank 0 at N=1 only: the fp64 oracle on
+    # a bounded sample of seeded rows of every head (about 2.5e11 flops, 10-20 s on the host);
+    # its outputs also give the line's parity check of the timed path on those rows
+    cpu_base, ref_rows = None, None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
-        secs, fl = time_oracle(w, 4096, range(w.Hq), threads)
+        n_rows = rows_for_budget(w, 2.5e11)
+        secs, fl, ref_rows = time_oracle(w, n_rows, range(w.Hq), threads, qkv=(q, k, v))
+        full = algorithmic_flops(w)
         cpu_base = {"value": fl / secs / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
-                    "sample": f"4096 seeded query rows x {w.Hq} heads of the workload, fp64, {secs:.1f} s"}
+                    "cpu_model": cpu_model(),
+                    "sample": f"{n_rows} seeded query rows x {w.Hq} heads of batch 0 of the workload (forced rows "
+                              f"0, S-1 and partition edges), full key range, fp64, {secs:.1f} s",
+                    "sample_seconds": secs, "sample_flops": fl,
+                    "extrapolated_full_s": secs * full / fl,
+                    "extrapolation": "extrapolated: sample time x (visible pairs of the whole workload / visible "
+                                     "pairs of the sampled rows)"}
 
-    q, k, v = make_qkv(w)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     if args.plan == "ring":
         plan = m.mesh_attn_plan_create_ring(w.S, w.P, w.causal)
@@ -455,10 +513,30 @@ def main():
     flops = algorithmic_flops(w)
     value = job_throughput(ws, flops, ms_per_step)
 
-    # backward pass on the same workload (a separate object of the line; not part of `value`)
+    # parity of the timed path's output on the oracle's sampled rows
+    parity = None
+    if ref_rows is not None:
+        to, tl = (2e-2, 1e-3) if w.dtype == "bf16" else (1e-4, 1e-4)
+        eo = el = 0.0
+        finite = True
+        for h, (rows_h, o_ref, l_ref) in ref_rows.items():
+            idx = torch.as_tensor(rows_h, device=dev)
+            og = O[0, h].index_select(0, idx).double().cpu()
+            lg = LSE[0, h].index_select(0, idx).double().cpu()
+            finite = finite and bool(torch.isfinite(og).all()) and bool(torch.isfinite(lg).all())
+            eo = max(eo, (og - o_ref).abs().max().item())
+            el = max(el, (lg - l_ref).abs().max().item())
+        parity = {"rows": f"{len(next(iter(ref_rows.values()))[0])} seeded rows x {len(ref_rows)} heads (batch 0), "
+                          "the cpu_baseline sample", "max_abs_err_O": eo, "max_abs_err_LSE": el,
+                  "tol_O": to, "tol_LSE": tl, "pass": finite and eo <= to and el <= tl}
+    del po, pl, O, LSE
+    torch.cuda.empty_cache()
+
+    # backward pass on its own workload (a separate object of the line; not part of `value`)
     bwd = None
     if not args.no_backward:
-        bwd = run_backward(m, w, plan, qd, kd, vd, O, LSE, dev, args, stream, flops)
+        bwd = run_backward(m, WORKLOADS[args.backward_workload], dev, args, stream)
+        torch.cuda.empty_cache()
 
     # end to end through the public call, host buffers in pinned memory
     e2e = None
@@ -485,11 +563,17 @@ def main():
         # counters only describe the kernel they were taken on
         if rec and sha.startswith(rec["source_sha256_prefix"]):
             traffic = rec["bytes"]
+    # A timed region of a second or more runs the tile kernel back to back under the power cap:
+    # its denominator is then the sustained (seconds-long) GEMM rate, else the burst rate.
+    sustained = total_ms >= 1000.0 and bool(peaks.get("bf16_tflops_sustained"))
+    peak_bf16 = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     if w.dtype == "bf16":
-        roof = {"bound": "tensor", "achieved": tile_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": tile_tflops / peaks["bf16_tflops"], "traffic": traffic,
-                "kernel": "tile_fwd_tc_kernel", "peak_kind": f"{peak_kind} bf16 dense burst"}
-        if peaks.get("bf16_tflops_sustained"):  # context: the power-capped, seconds-long GEMM rate
+        roof = {"bound": "tensor", "achieved": tile_tflops, "peak": peak_bf16, "unit": "TFLOP/s",
+                "frac": tile_tflops / peak_bf16, "traffic": traffic,
+                "kernel": "tile_fwd_tc_kernel",
+                "peak_kind": f"{peak_kind} bf16 dense {'sustained' if sustained else 'burst'}",
+                "frac_of_burst": tile_tflops / peaks["bf16_tflops"]}
+        if peaks.get("bf16_tflops_sustained"):
             roof["frac_of_sustained"] = tile_tflops / peaks["bf16_tflops_sustained"]
         exe = executed_flops_fwd(m, plan, w)
         roof["executed_tflops"] = exe / (tile_ms * 1e-3) / 1e12  # full blocks, masked halves included
@@ -498,11 +582,12 @@ def main():
     else:
         # fp32 inputs: every product is six bf16 tensor-core products of the operands' exact
         # three-piece split, so the ceiling for the fp32 rate is the bf16 peak / 6
-        peak32 = peaks["bf16_tflops"] / 6
+        peak32 = peak_bf16 / 6
         roof = {"bound": "tensor", "achieved": tile_tflops, "peak": peak32, "unit": "TFLOP/s",
                 "frac": tile_tflops / peak32, "traffic": None,
                 "kernel": "split_kernel + tile_fwd_tc32_kernel",
-                "peak_kind": f"{peak_kind} bf16 dense burst / 6 (six bf16 products per fp32 product)"}
+                "peak_kind": f"{peak_kind} bf16 dense {'sustained' if sustained else 'burst'} / 6 "
+                             "(six bf16 products per fp32 product)"}
         launches_per_step = 3  # split, tile, merge
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -514,7 +599,7 @@ def main():
                   "frac": merge_gbs / peaks["hbm_gbs"], "bytes_per_launch": mbytes, "ms": merge_ms},
         "tile_fwd_ms": tile_ms, "merge_ms": merge_ms, "plan_ms": plan_ms, "backward": bwd,
         "comm_counted": counted_volumes(m, w),
-        "cpu_baseline": cpu_base, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+        "parity": parity, "cpu_baseline": cpu_base, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)

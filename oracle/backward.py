@@ -118,14 +118,25 @@ def attention_bwd_bhsd(Q, K, V, dO, causal: bool, scale: Optional[float] = None,
     return dQ, dK, dV, LSE, D
 
 
-def dq_rows(Q, K, V, dO, causal: bool, rows, scale: Optional[float] = None) -> torch.Tensor:
+def _forward_with_magnitude(q, pos, k64, v64, do, scale: float, causal: bool):
+    """Forward of rows q at positions pos with values [v, |v|] in one pass: LSE, D = dO . O and
+    the rows' magnitude of D, dmag = sum_e |dO_e| (|O_e| + sum_j P_j |v_je|)."""
+    dv = v64.shape[1]
+    o2, lse = attention_rows(q, pos, k64, torch.cat([v64, v64.abs()], dim=1), scale, causal)
+    o, o_abs = o2[:, :dv], o2[:, dv:]
+    return lse, (do * o).sum(dim=-1), (do.abs() * (o.abs() + o_abs)).sum(dim=-1)
+
+
+def dq_rows(Q, K, V, dO, causal: bool, rows, scale: Optional[float] = None, absolute: bool = False):
     """dQ on sampled query rows only: rows is an int array [B, Hq, n].  Each row needs only its
-    own forward (LSE_i, O_i, hence D_i) and all keys.  Returns dQ [B, Hq, n, d] in fp64."""
+    own forward (LSE_i, O_i, hence D_i) and all keys.  Returns dQ [B, Hq, n, d] in fp64; with
+    absolute=True also the rows' magnitude sums of bwd_rows (a second tensor of the same shape)."""
     B, Hq, S, d = Q.shape
     Hkv = K.shape[1]
     g = Hq // Hkv
     scale = default_scale(d) if scale is None else scale
     out = torch.empty(B, Hq, rows.shape[-1], d, dtype=F64)
+    mag = torch.empty_like(out) if absolute else None
     for b in range(B):
         for kh in range(Hkv):
             k64, v64 = _as64(K[b, kh]), _as64(V[b, kh])
@@ -133,7 +144,40 @@ def dq_rows(Q, K, V, dO, causal: bool, rows, scale: Optional[float] = None) -> t
                 pos = torch.as_tensor(rows[b, h], dtype=torch.int64)
                 q = _as64(Q[b, h])[pos]
                 do = _as64(dO[b, h])[pos]
-                o, lse = attention_rows(q, pos, k64, v64, scale, causal)
-                dsum = (do * o).sum(dim=-1)
+                lse, dsum, dmag = _forward_with_magnitude(q, pos, k64, v64, do, scale, causal)
                 out[b, h], _, _ = bwd_rows(q, pos, k64, v64, do, lse, dsum, scale, causal, want_kv=False)
-    return out
+                if absolute:
+                    mag[b, h], _, _ = bwd_rows(q, pos, k64, v64, do, lse, dsum, scale, causal, want_kv=False,
+                                               absolute=True, dmag=dmag)
+    return (out, mag) if absolute else out
+
+
+def dkdv_keys(Q, K, V, dO, causal: bool, b: int, kh: int, keys, scale: Optional[float] = None,
+              row_chunk: int = 4096):
+    """dK and dV of KV head kh (batch b) on the sampled key rows `keys` (global positions), with
+    the magnitude sums of bwd_rows.  A key's gradient sums over every query row that sees it, in
+    every query head of the group, so this needs the forward (LSE_i, D_i, dmag_i) of all rows
+    of those heads.  Returns (dk, dv, dk_mag, dv_mag), each [n_keys, d] in fp64."""
+    B, Hq, S, d = Q.shape
+    g = Hq // K.shape[1]
+    scale = default_scale(d) if scale is None else scale
+    keys = torch.as_tensor(keys, dtype=torch.int64)
+    k64, v64 = _as64(K[b, kh]), _as64(V[b, kh])
+    ks, vs = k64[keys], v64[keys]
+    dk = torch.zeros(len(keys), d, dtype=F64)
+    dv = torch.zeros(len(keys), V.shape[-1], dtype=F64)
+    dk_mag, dv_mag = torch.zeros_like(dk), torch.zeros_like(dv)
+    for h in range(kh * g, (kh + 1) * g):
+        for r0 in range(0, S, row_chunk):
+            pos = torch.arange(r0, min(S, r0 + row_chunk))
+            q = _as64(Q[b, h])[pos]
+            do = _as64(dO[b, h])[pos]
+            lse, dsum, dmag = _forward_with_magnitude(q, pos, k64, v64, do, scale, causal)
+            _, a, c = bwd_rows(q, pos, ks, vs, do, lse, dsum, scale, causal, key_pos=keys)
+            dk += a
+            dv += c
+            _, a, c = bwd_rows(q, pos, ks, vs, do, lse, dsum, scale, causal, key_pos=keys, absolute=True,
+                               dmag=dmag)
+            dk_mag += a
+            dv_mag += c
+    return dk, dv, dk_mag, dv_mag

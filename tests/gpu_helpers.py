@@ -12,6 +12,27 @@ from oracle import attention as OA
 # tolerances of the comparison against the fp64 oracle (max absolute error)
 TOL = {"f32": (1e-4, 1e-4), "bf16": (2e-2, 1e-3)}
 
+# unit roundoff of bf16: 8 significant bits, round to nearest even
+U_BF16 = 2.0 ** -8
+
+
+def bf16_grad_bound(ref, mag, n_terms: int):
+    """Elementwise error bound of a gradient computed from bf16 inputs, derived term by term from
+    the arithmetic of the tile backward (ref: the fp64 oracle's gradient, mag: the oracle's
+    magnitude sums for it, n_terms: the most products one element sums).
+
+    * u |ref|: the result is rounded to bf16 once.
+    * u mag: the products take P (dV) and dS (dQ, dK) rounded to bf16 once, and D from the
+      forward's bf16 O; mag carries exactly these terms (scale sum (|dS| + dmag P) |k| for dQ,
+      the transposed sum for dK, sum P |dO| for dV).
+    * 2^-9 mag: P is recomputed from the forward's LSE, which is within 1e-3 of the exact one
+      (the forward's LSE tolerance), so P is off by a relative 1e-3; the fp32 recomputation of
+      the scores and of dP over d <= 128 exact bf16 products adds under 2^-16 relative.
+    * n 2^-23 mag: fp32 accumulation of n terms, worst case with adders that truncate (one ulp,
+      2^-23 relative, per addition).
+    Plus 1e-6 absolute for elements whose terms all cancel."""
+    return U_BF16 * ref.abs() + (U_BF16 + 2.0 ** -9 + n_terms * 2.0 ** -23) * mag + 1e-6
+
 
 def run_gpu(lib, w, q, k, v, kvr=None, greedy=None):
     """Whole path through the binding; returns device tensors O, LSE, partial O, partial LSE and the plan."""

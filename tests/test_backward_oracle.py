@@ -196,3 +196,58 @@ def test_magnitude_sums_bound_the_gradients(causal):
     O, _ = OA.attention_bhsd(Q, K, Vp, causal)
     mp = OB.attention_bwd_bhsd(Q, K, Vp, dOp, causal, absolute=True)
     assert torch.allclose(mp[4], 2 * (dOp * O).sum(dim=-1), atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_key_and_row_gradients_match_full(causal):
+    """dkdv_keys (dK, dV on chosen key rows, with magnitudes) and dq_rows with magnitudes equal
+    the full backward (itself pinned above by finite differences and autograd) on those rows."""
+    Q, K, V, dO = _case(1, 4, 2, 37, 8, 41)
+    dQ, dK, dV, _, _ = OB.attention_bwd_bhsd(Q, K, V, dO, causal)
+    mQ, mK, mV, _, _ = OB.attention_bwd_bhsd(Q, K, V, dO, causal, absolute=True)
+    keys = [0, 5, 17, 36]
+    for kh in range(2):
+        dk, dv, mk, mv = OB.dkdv_keys(Q, K, V, dO, causal, 0, kh, keys, row_chunk=16)
+        for got, ref in ((dk, dK[0, kh, keys]), (dv, dV[0, kh, keys]), (mk, mK[0, kh, keys]), (mv, mV[0, kh, keys])):
+            assert torch.allclose(got, ref, atol=1e-12, rtol=1e-12)
+    import numpy as np
+    rows = np.array([[[0, 3, 36], [1, 2, 30], [4, 9, 33], [0, 20, 36]]])
+    got, mag = OB.dq_rows(Q, K, V, dO, causal, rows, absolute=True)
+    for h in range(4):
+        assert torch.allclose(got[0, h], dQ[0, h, rows[0, h]], atol=1e-12, rtol=1e-12)
+        assert torch.allclose(mag[0, h], mQ[0, h, rows[0, h]], atol=1e-12, rtol=1e-12)
+
+
+def test_bf16_gradient_bound_rejects_one_missing_block():
+    """The elementwise bound of the bf16 GPU gradients is tight enough to catch the loss of a
+    single 128-wide block of the sum: on a bf16-rounded causal case (S = 2048, d = 128), dropping
+    one key block from dQ, or one query block from dK and dV, moves some element outside the
+    bound -- also among rows and keys at least 512 positions away from the dropped block, where
+    the block is a small share of the sum.  (The perturbation is made on the oracle's result.)"""
+    from mesh_inputs import Workload, make_do, make_qkv
+    from tests.gpu_helpers import bf16_grad_bound
+    w = Workload(150, "bound_check", 1, 1, 1, 2048, 128, "bf16", True, 4)
+    q, k, v = make_qkv(w)
+    dO = make_do(w)
+    rQ, rK, rV, LSE, D = OB.attention_bwd_bhsd(q, k, v, dO, True)
+    mQ, mK, mV, _, _ = OB.attention_bwd_bhsd(q, k, v, dO, True, absolute=True)
+    Q64, K64, V64, G64 = (t[0, 0].double() for t in (q, k, v, dO))
+    pos = torch.arange(w.S)
+    scale = 1.0 / math.sqrt(w.d)
+    for blk in (0, 3, 8):
+        span = torch.arange(blk * 128, (blk + 1) * 128)
+        # dQ without key block blk: the error is that block's contribution
+        drop_q, _, _ = OB.bwd_rows(Q64, pos, K64[span], V64[span], G64, LSE[0, 0], D[0, 0], scale, True,
+                                   key_pos=span, want_kv=False)
+        ratio_q = drop_q.abs() / bf16_grad_bound(rQ[0, 0], mQ[0, 0], w.S)
+        far_rows = pos >= (blk + 1) * 128 + 512
+        assert ratio_q.max() > 1.0 and ratio_q[far_rows].max() > 1.0, (blk, ratio_q[far_rows].max())
+        # dK and dV without query block blk
+        _, drop_k, drop_v = OB.bwd_rows(Q64[span], span, K64, V64, G64[span], LSE[0, 0, span], D[0, 0, span],
+                                        scale, True)
+        ratio_k = drop_k.abs() / bf16_grad_bound(rK[0, 0], mK[0, 0], w.S)
+        ratio_v = drop_v.abs() / bf16_grad_bound(rV[0, 0], mV[0, 0], w.S)
+        assert ratio_k.max() > 1.0 and ratio_v.max() > 1.0, blk
+        if blk >= 8:
+            far_keys = pos < blk * 128 - 512
+            assert ratio_k[far_keys].max() > 1.0 and ratio_v[far_keys].max() > 1.0, blk

@@ -8,11 +8,12 @@ import torch
 
 from mesh_inputs import WORKLOADS, Workload, make_do, make_qkv
 from oracle import backward as OB
+from tests.gpu_helpers import bf16_grad_bound
 
 
 pytestmark = pytest.mark.gpu
 
-# fp32: the fp32 tolerance of the forward (1e-4 absolute).  bf16: see bf16_bound.
+# fp32: the fp32 tolerance of the forward (1e-4 absolute).  bf16: bf16_grad_bound, elementwise.
 F32_CASES = [
     WORKLOADS["tiny_f32"],
     Workload(140, "f32_bwd_causal_ragged_L100", 1, 2, 1, 900, 128, "f32", True, 9),
@@ -41,22 +42,18 @@ def run_backward(lib, w, q, k, v, dO, plan=None):
     return out, plan, LSE
 
 
-def bf16_bound(ref, mag):
-    """Elementwise error bound of a bf16 gradient, derived from the arithmetic.  bf16 keeps 8
-    significant bits, so rounding to nearest moves a value by at most u = 2^-8 of itself.  The
-    products take P (for dV) and dS (for dQ, dK) rounded to bf16, and D comes from the forward's
-    bf16 O (off by at most u dmag); so a gradient is off by at most u mag (mag: the oracle's
-    magnitude sums, which carry both terms), and the result is rounded to bf16 once more
-    (u |ref|).  The bound is twice that, plus 1e-6 for fp32 accumulation."""
-    return 2.0 ** -7 * (mag + ref.abs()) + 1e-6
+def n_terms(w, grad: str) -> int:
+    """Most products one gradient element sums: the keys of a query row (dQ), the query rows of
+    every head of the group (dK, dV)."""
+    return w.S if grad == "dQ" else w.S * (w.Hq // w.Hkv)
 
 
-def compare(w, got, ref, mag):
+def compare(w, got, ref, mag, n):
     """(max |err|, max err / bound) of one gradient tensor."""
     e = (got.double().cpu() - ref).abs()
     if w.dtype == "f32":
         return e.max().item(), e.max().item() / 1e-4
-    return e.max().item(), (e / bf16_bound(ref, mag)).max().item()
+    return e.max().item(), (e / bf16_grad_bound(ref, mag, n)).max().item()
 
 
 def check_gradients(w, got, q, k, v, dO, tag=""):
@@ -64,7 +61,7 @@ def check_gradients(w, got, q, k, v, dO, tag=""):
     rQ, rK, rV, _, _ = OB.attention_bwd_bhsd(q, k, v, dO, w.causal)
     mags = OB.attention_bwd_bhsd(q, k, v, dO, w.causal, absolute=True)[:3] if w.dtype == "bf16" else (None,) * 3
     for name, g, r, m in (("dQ", dQ, rQ, mags[0]), ("dK", dK, rK, mags[1]), ("dV", dV, rV, mags[2])):
-        e, ratio = compare(w, g, r, m)
+        e, ratio = compare(w, g, r, m, n_terms(w, name))
         print(f"[parity-bwd] {w.name}{tag} {name}: max|err| = {e:.3e}, max err/bound = {ratio:.3f} "
               f"(max|ref| {r.abs().max().item():.3e})")
         assert ratio <= 1.0, f"{w.name} {name}: error {ratio:.3f}x the bound"
@@ -90,9 +87,9 @@ def check_backward_partials(lib, w, plan, got, q, k, v, dO, LSE):
     scale = 1.0 / math.sqrt(d)
     bf = w.dtype == "bf16"
 
-    def ok(got_, ref_, mag_):
+    def ok(got_, ref_, mag_, n):
         e = (got_.double() - ref_).abs()
-        return bool((e <= (bf16_bound(ref_, mag_) if bf else 1e-4)).all())
+        return bool((e <= (bf16_grad_bound(ref_, mag_, n) if bf else 1e-4)).all())
 
     for b in range(B):
         for hk in range(Hkv):
@@ -111,7 +108,7 @@ def check_backward_partials(lib, w, plan, got, q, k, v, dO, LSE):
                     r, _, _ = OB.bwd_rows(*args, key_pos=keys, want_kv=False)
                     m = OB.bwd_rows(*args, key_pos=keys, want_kv=False, absolute=True,
                                     dmag=DM64[b, h, rows])[0] if bf else None
-                    assert ok(dq_p[b, h, slot], r, m), f"dq slot {slot} (p={p}, t={t})"
+                    assert ok(dq_p[b, h, slot], r, m, n_terms(w, "dQ")), f"dq slot {slot} (p={p}, t={t})"
                 for (kk, t, slot), ql in zip(kv_items, kv_q):
                     keys = torch.arange(kk * L, (kk + 1) * L)
                     rows = torch.cat([torch.arange(x * L, (x + 1) * L) for x in ql])
@@ -124,9 +121,10 @@ def check_backward_partials(lib, w, plan, got, q, k, v, dO, LSE):
                         _, mk, mv = OB.bwd_rows(*args, key_pos=keys, absolute=True, dmag=DM64[b, h, rows])
                         mag_k[slot] += mk
                         mag_v[slot] += mv
+            nk = n_terms(w, "dK")
             for (kk, t, slot) in kv_items:
-                assert ok(dk_p[b, hk, slot], acc_k[slot], mag_k[slot]), f"dk slot {slot} (k={kk}, t={t})"
-                assert ok(dv_p[b, hk, slot], acc_v[slot], mag_v[slot]), f"dv slot {slot} (k={kk}, t={t})"
+                assert ok(dk_p[b, hk, slot], acc_k[slot], mag_k[slot], nk), f"dk slot {slot} (k={kk}, t={t})"
+                assert ok(dv_p[b, hk, slot], acc_v[slot], mag_v[slot], nk), f"dv slot {slot} (k={kk}, t={t})"
 
 
 @pytest.mark.parametrize("w", F32_CASES, ids=lambda w: w.name)
@@ -186,13 +184,37 @@ def test_backward_bf16_plan_variants(lib):
     check_gradients(w, got, q, k, v, dO, tag=" ring")
 
 
+def test_backward_bf16_several_units_per_cta(lib):
+    """A mid-size case whose persistent backward kernels take several units per CTA: with
+    P = 16 partitions of 512 tokens and 4 heads the dK/dV kernel has 640 units and the dQ kernel
+    928, against one CTA per SM.  So the cross-unit code (the next unit's resident loads, the
+    drain and overwrite barriers, barrier phases counted over a CTA's whole sequence of blocks)
+    runs under an elementwise check of dQ, dK and dV and of every partial slot."""
+    w = Workload(157, "bf16_bwd_multi_unit", 1, 4, 4, 8192, 128, "bf16", True, 16)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    q, k, v = make_qkv(w)
+    dO = make_do(w)
+    got, plan, LSE = run_backward(lib, w, q, k, v, dO)
+    blocks = plan.L // 128
+    units_dkdv = plan.n_kv_slots * w.B * w.Hkv * blocks
+    units_dq = plan.n_slots * w.B * w.Hq * blocks
+    print(f"[parity-bwd] {w.name}: {units_dkdv} dK/dV units, {units_dq} dQ units, {sms} SMs")
+    assert units_dkdv >= 4 * sms and units_dq >= 6 * sms
+    check_gradients(w, got, q, k, v, dO)
+    check_backward_partials(lib, w, plan, got, q, k, v, dO, LSE)
+
+
 @pytest.mark.parametrize("name", ["bf16_causal_16k", "gqa_causal_64k"])
 def test_backward_full_size(lib, name):
-    """Full-size workloads (the forward's bench configurations): dQ on seeded sampled rows against
-    the oracle one row at a time, and two identities that hold at any size for every KV head and
-    column: sum_j dK_j = scale sum_i q_i sum_j dS_ij = 0 and sum_j dV_j = sum_i dO_i (rows of P sum
-    to 1), each within 2^-7 of the sum of the terms' magnitudes."""
+    """Full-size workloads (the forward's bench configurations), elementwise on seeded samples:
+    dQ on sampled query rows (each needs only its own forward row), and on the bf16 causal 16K
+    workload dK and dV on sampled key rows of two KV heads (each sums over every query row that
+    sees it, so the oracle runs the forward of all rows of those heads), all against the derived
+    bound.  Besides, two identities that hold at any size for every KV head and column:
+    sum_j dK_j = scale sum_i q_i sum_j dS_ij = 0 and sum_j dV_j = sum_i dO_i (rows of P sum to 1),
+    each within 2^-7 of the sum of the terms' magnitudes."""
     import numpy as np
+    from mesh_inputs import forced_rows
     w = WORKLOADS[name]
     q, k, v = make_qkv(w)
     dO = make_do(w)
@@ -208,19 +230,32 @@ def test_backward_full_size(lib, name):
     dv_abs = dV.abs().sum(dim=2)
     assert ((dv_sum - want).abs() <= 2.0 ** -7 * dv_abs + 1e-3).all()
     rng = np.random.default_rng(w.cfg_id)
-    rows = np.stack([np.stack([np.sort(rng.choice(w.S, 24, replace=False)) for _ in range(w.Hq)])
-                     for _ in range(w.B)])
-    rows[..., 0] = 0
-    rows[..., -1] = w.S - 1
-    ref = OB.dq_rows(q, k, v, dO, w.causal, rows)
+    forced = np.array(forced_rows(w.S, w.P))
+    pool = np.setdiff1d(np.arange(w.S), forced)
+
+    def draw(n):
+        return np.sort(np.concatenate([forced, rng.choice(pool, n - len(forced), replace=False)]))
+
+    rows = np.stack([np.stack([draw(24) for _ in range(w.Hq)]) for _ in range(w.B)])
+    ref, mag = OB.dq_rows(q, k, v, dO, w.causal, rows, absolute=True)
     got_rows = torch.stack([torch.stack([dQ[b, h, torch.as_tensor(rows[b, h])] for h in range(w.Hq)])
                             for b in range(w.B)])
-    e = (got_rows - ref).abs()
-    # the rows' magnitude bound would need the full forward; use 2^-7 of the row's largest value
-    bound = 2.0 ** -7 * ref.abs().amax(dim=-1, keepdim=True) + 2e-3
-    print(f"[parity-bwd] {name} sampled dQ rows: max|err| = {e.max().item():.3e}, "
-          f"max err/bound = {(e / bound).max().item():.3f}")
-    assert (e <= bound).all()
+    r = ((got_rows - ref).abs() / bf16_grad_bound(ref, mag, n_terms(w, "dQ"))).max().item()
+    print(f"[parity-bwd] {name} sampled dQ rows: max|err| = {(got_rows - ref).abs().max().item():.3e}, "
+          f"max err/bound = {r:.3f}")
+    assert r <= 1.0
+    if name != "bf16_causal_16k":
+        return
+    for hk in (0, w.Hkv - 5):
+        keys = draw(32)
+        rk, rv, mk, mv = OB.dkdv_keys(q, k, v, dO, w.causal, 0, hk, keys)
+        idx = torch.as_tensor(keys)
+        for nm, got_k, ref_k, mag_k in (("dK", dK[0, hk, idx], rk, mk), ("dV", dV[0, hk, idx], rv, mv)):
+            e = (got_k - ref_k).abs()
+            r = (e / bf16_grad_bound(ref_k, mag_k, n_terms(w, nm))).max().item()
+            print(f"[parity-bwd] {name} KV head {hk} sampled {nm} rows: max|err| = {e.max().item():.3e}, "
+                  f"max err/bound = {r:.3f}")
+            assert r <= 1.0, f"{nm} of KV head {hk}: {r:.3f}x the bound"
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
