@@ -70,6 +70,11 @@ WORKLOADS: Dict[str, Workload] = {
                                  sampled_rows=4096),
     "stress_256k": Workload(5, "stress_256k", 1, 16, 4, 262144, 128, "bf16", True, 1024,
                             k_scale=4.0, sampled_rows=4096),
+    # a profiling-size slice of the stress workload: the same partition length (256 tokens),
+    # GQA group (4), K scaling and mask, with a quarter of the sequence and half of the heads,
+    # so that a replayed counter capture holds about 4 GB on the device
+    "stress_64k": Workload(6, "stress_64k", 1, 8, 2, 65536, 128, "bf16", True, 256,
+                           k_scale=4.0, sampled_rows=4096),
 }
 
 

@@ -63,13 +63,16 @@ def test_growing_and_shrinking_scores(lib, ramp, causal):
     block, so the running reference of the online softmax is raised (and O and l rescaled) many
     times inside one work unit.  Shrinking: the first block holds the maximum and later blocks
     only add small terms.  The growing ramp makes attention so peaked that O is close to single
-    rows of V (|V| < 8 for these draws), whose bf16 rounding (half an ulp, at most 2^-6 below 8)
-    stays inside the 2e-2 tolerance, while a wrong rescale factor would be off by O(|O|)."""
+    rows of V, and with |V| up to 4.7 the two roundings the bf16 path makes add up past the
+    absolute 2e-2: O rounded to bf16 (half an ulp, 2^-6 for |O| in [4, 8)) plus P rounded to
+    bf16 in the PV product (2^-9 of the second-largest weight times |V|); unscaled the worst row
+    measures 2.11e-2.  V is scaled by 1/4 (exact in bf16), which scales both roundings by 1/4,
+    while a wrong rescale factor would still be off by O(|O|)."""
     w = Workload(117, "bf16_ramp", 1, 2, 1, 4096, 128, "bf16", causal, 4)
     q, k, v = make_qkv(w)
-    assert v.abs().max().item() < 8.0
     ramp_k = 1.0 + ramp * torch.arange(w.S, dtype=torch.float32) / w.S
     k = (k.float() * ramp_k[None, None, :, None]).to(k.dtype)
+    v = v * 0.25
     O, LSE, po, pl, plan = run_gpu(lib, w, q, k, v)
     check_full(w, O, LSE, q, k, v)
     check_partials(lib, w, plan, po, pl, q, k, v)
