@@ -43,7 +43,8 @@ def executed_flops_fwd(m, plan, w) -> float:
     half of causal diagonal blocks and the padding of a ragged last block (a diagnostic beside
     the algorithmic count).  A unit is a pair of 128-row query tiles of one work item, and it
     visits every 128-key block of the item's KV partitions up to its last tile on the causal
-    diagonal partition."""
+    diagonal partition.  At d = 128 the pair's products always span 256 rows (M = 256 on two
+    SMs), also when the partition has a single 128-row tile."""
     items, _, kvs = m.mesh_attn_plan_order(plan)
     nb = -(-w.L // 128)
     per_item = 0
@@ -52,7 +53,7 @@ def executed_flops_fwd(m, plan, w) -> float:
             ntiles = min(2, nb - a0)
             a_max = a0 + ntiles - 1
             blocks = sum(min(nb, a_max + 1) if (w.causal and k == p) else nb for k in kl)
-            per_item += blocks * ntiles
+            per_item += blocks * (2 if w.d == 128 else ntiles)
     return 4.0 * 128 * 128 * w.d * per_item * w.B * w.Hq
 
 
@@ -96,6 +97,13 @@ def merge_bytes(w, n_slots: int) -> float:
     read = n_slots * w.L * w.Hq * w.B * (4 * w.d + 4)
     write = w.B * w.Hq * w.S * (es * w.d + 4)
     return float(read + write)
+
+
+def kernel_sources(w):
+    """Source files whose content the tile kernel's DRAM counters describe: the bf16 kernel for the
+    workload's head dimension, the inline-PTX helpers and the planner (it fixes the launch order)."""
+    kern = "tile_fwd_tc2.cu" if w.d == 128 else "tile_fwd_tc.cu"
+    return (kern, "ptx.cuh", "planner.cpp")
 
 
 def load_peaks():
@@ -556,7 +564,7 @@ def main():
         with open(prof) as f:
             rec = json.load(f).get(w.name, {}).get("tile_fwd")
         h = hashlib.sha256()
-        for name in ("tile_fwd_tc.cu", "ptx.cuh"):  # the kernel and the inline-PTX helpers it uses
+        for name in kernel_sources(w):  # the kernel, its inline-PTX helpers and the planner's order
             with open(os.path.join(ROOT, "tiled_distributed_attention_gb300", "csrc", name), "rb") as f:
                 h.update(f.read())
         sha = h.hexdigest()
@@ -570,7 +578,7 @@ def main():
     if w.dtype == "bf16":
         roof = {"bound": "tensor", "achieved": tile_tflops, "peak": peak_bf16, "unit": "TFLOP/s",
                 "frac": tile_tflops / peak_bf16, "traffic": traffic,
-                "kernel": "tile_fwd_tc_kernel",
+                "kernel": "tile_fwd_tc2_kernel" if w.d == 128 else "tile_fwd_tc_kernel",
                 "peak_kind": f"{peak_kind} bf16 dense {'sustained' if sustained else 'burst'}",
                 "frac_of_burst": tile_tflops / peaks["bf16_tflops"]}
         if peaks.get("bf16_tflops_sustained"):

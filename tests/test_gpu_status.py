@@ -32,7 +32,7 @@ def test_wait_timeout_reports_status_and_context_survives(lib):
     finally:
         lib.mesh_attn_set_wait_limit_ns(2_000_000_000)
     assert code == 5, f"status block {st.tolist()}"
-    assert st[1].item() in (1, 2, 3)  # softmax, MMA or load role gave up
+    assert st[1].item() in (1, 2, 3, 5)  # softmax, MMA, load or relay role gave up
     # a set status makes later kernels skip their work
     lib.mesh_attn_merge(plan, 1, 2, 128, po, pl, O, LSE, ws, st)
     assert lib.mesh_attn_read_status(st) == 5

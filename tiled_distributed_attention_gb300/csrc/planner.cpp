@@ -181,11 +181,24 @@ void build_plan(Plan& pl, int64_t S, int32_t P, bool causal, bool kvr, bool gree
     pl.kv_off[i] = (int32_t)pos;
     std::copy(kv_scratch.begin() + k.kv_begin, kv_scratch.begin() + k.kv_begin + k.n_kv,
               pl.kv_list.begin() + pos);
-    pl.dev_items[i] = DevItem{k.p, k.slot, (int32_t)pos, k.n_kv};
     pos += k.n_kv;
   }
   pl.kv_off[n] = (int32_t)pos;
   if (pos != pl.n_live) throw std::logic_error("planner: KV entries do not cover the live blocks");
+  // The kernels' copy of the work list takes the tiles one after another (row-major over the
+  // mesh), each tile's items in that virtual device's greedy order.  The greedy pass fixes the
+  // order within each device; how the devices' sequences interleave on one GPU is free, and
+  // tile-major keeps a tile's KV set (shared by its items) and its mesh row's Q partitions
+  // (shared with the next tile of the row) in L2.
+  std::vector<int32_t> launch(n);
+  std::iota(launch.begin(), launch.end(), 0);
+  std::stable_sort(launch.begin(), launch.end(), [&](int32_t a, int32_t b) {
+    return std::tie(keys[a].t, keys[a].step, keys[a].p) < std::tie(keys[b].t, keys[b].step, keys[b].p);
+  });
+  for (int32_t j = 0; j < n; ++j) {
+    const Key& k = keys[launch[j]];
+    pl.dev_items[j] = DevItem{k.p, k.slot, pl.kv_off[launch[j]], k.n_kv};
+  }
   build_kv_slots(pl);
 }
 

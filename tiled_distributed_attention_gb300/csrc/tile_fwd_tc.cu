@@ -1,4 +1,5 @@
-// Tile attention forward on the 5th-generation tensor cores (sm_103a).
+// Tile attention forward on the 5th-generation tensor cores (sm_103a), one SM per unit: the
+// kernel for head dimension 64 (d = 128 runs on SM pairs, tile_fwd_tc2.cu).
 //
 // A work unit is (work item = (Q partition p, tile), batch b, query head h, pair of 128-row
 // query tiles of partition p).  For each unit the kernel visits the item's KV partitions in
@@ -656,7 +657,7 @@ static int launch(const TileArgs& a, void* stream, std::string* err) {
 }  // namespace tc
 
 int launch_tile_fwd_tc(const TileArgs& a, void* stream, std::string* err) {
-  if (a.d == 128) return tc::launch<128>(a, stream, err);
+  if (a.d == 128) return launch_tile_fwd_tc2(a, stream, err);  // SM pairs (tile_fwd_tc2.cu)
   if (a.d == 64) return tc::launch<64>(a, stream, err);
   *err = "tensor-core tile kernel supports d = 64 or 128";
   return (int)cudaErrorInvalidValue;
