@@ -43,8 +43,7 @@ def executed_flops_fwd(m, plan, w) -> float:
     half of causal diagonal blocks and the padding of a ragged last block (a diagnostic beside
     the algorithmic count).  A unit is a pair of 128-row query tiles of one work item, and it
     visits every 128-key block of the item's KV partitions up to its last tile on the causal
-    diagonal partition.  At d = 128 the pair's products always span 256 rows (M = 256 on two
-    SMs), also when the partition has a single 128-row tile."""
+    diagonal partition."""
     items, _, kvs = m.mesh_attn_plan_order(plan)
     nb = -(-w.L // 128)
     per_item = 0
@@ -53,7 +52,7 @@ def executed_flops_fwd(m, plan, w) -> float:
             ntiles = min(2, nb - a0)
             a_max = a0 + ntiles - 1
             blocks = sum(min(nb, a_max + 1) if (w.causal and k == p) else nb for k in kl)
-            per_item += blocks * (2 if w.d == 128 else ntiles)
+            per_item += blocks * ntiles
     return 4.0 * 128 * 128 * w.d * per_item * w.B * w.Hq
 
 
@@ -100,10 +99,9 @@ def merge_bytes(w, n_slots: int) -> float:
 
 
 def kernel_sources(w):
-    """Source files whose content the tile kernel's DRAM counters describe: the bf16 kernel for the
-    workload's head dimension, the inline-PTX helpers and the planner (it fixes the launch order)."""
-    kern = "tile_fwd_tc2.cu" if w.d == 128 else "tile_fwd_tc.cu"
-    return (kern, "ptx.cuh", "planner.cpp")
+    """Source files whose content the tile kernel's DRAM counters describe: the kernel, its
+    inline-PTX helpers and the planner (it fixes the launch order of the work items)."""
+    return ("tile_fwd_tc.cu", "ptx.cuh", "planner.cpp")
 
 
 def load_peaks():
@@ -557,7 +555,7 @@ def main():
     tile_tflops = flops / (tile_ms * 1e-3) / 1e12
     mbytes = merge_bytes(w, plan.n_slots)
     merge_gbs = mbytes / (merge_ms * 1e-3) / 1e9
-    traffic = None
+    traffic, traffic_note = None, None
     prof = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(prof):
         import hashlib
@@ -571,6 +569,7 @@ def main():
         # counters only describe the kernel they were taken on
         if rec and sha.startswith(rec["source_sha256_prefix"]):
             traffic = rec["bytes"]
+            traffic_note = rec.get("note")
     # A timed region of a second or more runs the tile kernel back to back under the power cap:
     # its denominator is then the sustained (seconds-long) GEMM rate, else the burst rate.
     sustained = total_ms >= 1000.0 and bool(peaks.get("bf16_tflops_sustained"))
@@ -578,11 +577,13 @@ def main():
     if w.dtype == "bf16":
         roof = {"bound": "tensor", "achieved": tile_tflops, "peak": peak_bf16, "unit": "TFLOP/s",
                 "frac": tile_tflops / peak_bf16, "traffic": traffic,
-                "kernel": "tile_fwd_tc2_kernel" if w.d == 128 else "tile_fwd_tc_kernel",
+                "kernel": "tile_fwd_tc_kernel",
                 "peak_kind": f"{peak_kind} bf16 dense {'sustained' if sustained else 'burst'}",
                 "frac_of_burst": tile_tflops / peaks["bf16_tflops"]}
         if peaks.get("bf16_tflops_sustained"):
             roof["frac_of_sustained"] = tile_tflops / peaks["bf16_tflops_sustained"]
+        if traffic_note:
+            roof["traffic_source"] = traffic_note
         exe = executed_flops_fwd(m, plan, w)
         roof["executed_tflops"] = exe / (tile_ms * 1e-3) / 1e12  # full blocks, masked halves included
         roof["executed_over_algorithmic"] = exe / flops

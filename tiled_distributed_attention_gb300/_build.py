@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmesh_attn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["planner.cpp", "abi.cu", "tile_fwd_tc.cu", "tile_fwd_tc2.cu", "tile_fwd_tc32.cu", "merge.cu", "noalloc.cu",
+SOURCES = ["planner.cpp", "abi.cu", "tile_fwd_tc.cu", "tile_fwd_tc32.cu", "merge.cu", "noalloc.cu",
            "tile_bwd_simt.cu", "tile_bwd_tc.cu", "bwd_aux.cu"]
 
 

@@ -79,8 +79,6 @@ struct TileArgs {
 };
 // Kernel launchers return a cudaError_t value as int; *err gets a message on failure.
 int launch_tile_fwd_tc(const TileArgs& a, void* stream, std::string* err);
-// d = 128 on CTA pairs (tcgen05.mma.cta_group::2); launch_tile_fwd_tc dispatches to it.
-int launch_tile_fwd_tc2(const TileArgs& a, void* stream, std::string* err);
 // fp32 inputs: split Q, K and V into bf16 pieces in a.pieces, then the tensor-core forward.
 int launch_tile_fwd_tc32(const TileArgs& a, void* stream, std::string* err);
 // Byte layout of the bf16 pieces of fp32 Q, K and V ([3][rows][d] each, 256-byte aligned parts).

@@ -292,127 +292,6 @@ __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// ---------------------------------------------------------------- clusters (CTA pairs)
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Address in the shared memory of CTA `rank` of this cluster of the object at local address addr.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-// Every thread of every CTA of the cluster (a hardware barrier: use only where all threads are
-// known to arrive, i.e. at kernel entry and exit; warps need not be converged).
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-// Arrive on an mbarrier of any CTA of the cluster (address from mapa_shared), ordering this
-// thread's earlier memory operations before the arrival at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
-}
-// 32-bit store to the shared memory of any CTA of the cluster.
-__device__ __forceinline__ void st_shared_cluster(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-// try_wait that also acquires what other CTAs of the cluster released with their arrivals.
-__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// mbar_wait with cluster-scope acquire (the phase may complete through arrivals of the peer CTA).
-__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, int64_t limit_ns, volatile int32_t* abort,
-                                             int32_t* status, int32_t role, int32_t unit) {
-  if (mbar_try_wait_cl(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    if (mbar_try_wait_cl(bar, parity)) return true;
-    if (*abort) return false;
-    if ((int64_t)(global_timer_ns() - t0) > limit_ns) {
-      *abort = 1;
-      record_error(status, MESH_ATTN_ERR_DEVICE_TIMEOUT, role, unit);
-      return false;
-    }
-  }
-}
-__device__ __forceinline__ bool mbar_wait_cl_warp(uint32_t bar, uint32_t parity, int64_t limit_ns,
-                                                  volatile int32_t* abort, int32_t* status, int32_t role,
-                                                  int32_t unit) {
-  if (__all_sync(0xffffffffu, mbar_try_wait_cl(bar, parity))) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    if (__all_sync(0xffffffffu, mbar_try_wait_cl(bar, parity))) return true;
-    if (__any_sync(0xffffffffu, *abort != 0)) return false;
-    if (__any_sync(0xffffffffu, (int64_t)(global_timer_ns() - t0) > limit_ns)) {
-      if ((threadIdx.x & 31) == 0) {
-        *abort = 1;
-        record_error(status, MESH_ATTN_ERR_DEVICE_TIMEOUT, role, unit);
-      }
-      __syncwarp();
-      return false;
-    }
-  }
-}
-
-// ---------------------------------------------------------------- tcgen05 on CTA pairs
-// All tcgen05 allocation, MMA and commit instructions of a kernel use one cta_group; these are
-// the cta_group::2 forms.  Allocation and deallocation are collective: one warp of each CTA of
-// the pair executes them with the same column count.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-// Pair MMA issued by the even CTA: D (both CTAs' TMEM at d_tmem, 128 rows each) (+)= A (each
-// CTA's own 128 rows) * B (each CTA holds N/2 of B's N rows or columns); warp-converged forms as
-// tc_mma_*_warp.
-__device__ __forceinline__ void tc2_mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                                uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void tc2_mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                                uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive once on the mbarrier at local address `bar` in every CTA of `cta_mask` when every
-// tcgen05 operation this thread issued so far has completed.
-__device__ __forceinline__ void tc2_commit_mc_warp(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
-          bar),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // Hardware base-2 exponential (MUFU), flushes denormal results to zero.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

@@ -1,5 +1,4 @@
-// Tile attention forward on the 5th-generation tensor cores (sm_103a), one SM per unit: the
-// kernel for head dimension 64 (d = 128 runs on SM pairs, tile_fwd_tc2.cu).
+// Tile attention forward on the 5th-generation tensor cores (sm_103a).
 //
 // A work unit is (work item = (Q partition p, tile), batch b, query head h, pair of 128-row
 // query tiles of partition p).  For each unit the kernel visits the item's KV partitions in
@@ -12,8 +11,8 @@
 // partial results back to the Q owner, which merges them).
 //
 // GB300 mapping: a persistent grid of one CTA per SM; 12 warps = 3 warpgroups.
-//   warp 9      producer: takes the next unit from a global counter (units are numbered in
-//               planned order, item-major), publishes it through a 2-slot ring in shared
+//   warp 9      producer: takes the next unit from a global counter (units are numbered
+//               KV-head-major over the plan's launch order), publishes it through a 2-slot ring in shared
 //               memory, then TMA-loads the unit's two Q tiles and streams K and V blocks
 //               (128 rows x 64 columns, 128-byte swizzle) through a 2-stage mbarrier ring.
 //   warp 8      MMA issuer (one elected lane of a converged warp): S_t = Q_t K^T and O_t += P_t V with
@@ -92,7 +91,10 @@ struct Params {
   int64_t wait_limit_ns;
 };
 
-// What every role derives from a unit index.
+// What every role derives from a unit index.  Units are numbered KV-head-major: (batch, KV head,
+// work item in the plan's launch order, query head of the group, tile pair), so the units running
+// at once on the grid share one KV head's partitions and the query heads of a group share them in
+// L2.
 struct Unit {
   int b, h, qp;
   DevItem it;
@@ -105,15 +107,19 @@ struct Unit {
 
 __device__ __forceinline__ Unit decode(int u, const Params& prm) {
   Unit x;
+  const int g = prm.Hq / prm.Hkv;
   x.qp = u % prm.n_pairs;
   u /= prm.n_pairs;
-  x.h = u % prm.Hq;
-  u /= prm.Hq;
-  x.b = u % prm.B;
-  const int item = u / prm.B;
+  const int gi = u % g;
+  u /= g;
+  const int item = u % prm.n_items;
+  u /= prm.n_items;
+  const int hk = u % prm.Hkv;
+  x.b = u / prm.Hkv;
+  x.h = hk * g + gi;
   x.it = prm.items[item];
-  x.ok = x.it.p >= 0 && x.it.p < prm.P && x.it.slot >= 0 && x.it.slot < prm.n_slots && x.it.n_kv >= 1 &&
-         x.it.kv_off >= 0;
+  x.ok = x.b < prm.B && x.it.p >= 0 && x.it.p < prm.P && x.it.slot >= 0 && x.it.slot < prm.n_slots &&
+         x.it.n_kv >= 1 && x.it.kv_off >= 0;
   x.nb = (int)((prm.L + BN - 1) / BN);
   x.a0 = 2 * x.qp;
   x.ntiles = ((int64_t)(x.a0 + 1) * BM < prm.L) ? 2 : 1;
@@ -657,7 +663,7 @@ static int launch(const TileArgs& a, void* stream, std::string* err) {
 }  // namespace tc
 
 int launch_tile_fwd_tc(const TileArgs& a, void* stream, std::string* err) {
-  if (a.d == 128) return launch_tile_fwd_tc2(a, stream, err);  // SM pairs (tile_fwd_tc2.cu)
+  if (a.d == 128) return tc::launch<128>(a, stream, err);
   if (a.d == 64) return tc::launch<64>(a, stream, err);
   *err = "tensor-core tile kernel supports d = 64 or 128";
   return (int)cudaErrorInvalidValue;
