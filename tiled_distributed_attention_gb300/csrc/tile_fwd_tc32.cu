@@ -65,8 +65,8 @@ struct Layout {
   static constexpr uint32_t KBOX = BN * 128;    // 64 rows x 64 bf16 columns
   static constexpr uint32_t Q_OFF = 0, K_OFF = 3 * QP, V_OFF = K_OFF + 3 * KP;
   static constexpr uint32_t BAR_OFF = V_OFF + 3 * KP;
-  static constexpr int B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 2, B_SFULL = 3, B_PFULL = 4, B_OFULL = 5, B_DRAIN = 6,
-                       NBARS = 7;
+  static constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 2, B_VFULL = 3, B_VEMPTY = 4, B_SFULL = 5, B_PFULL = 6,
+                       B_OFULL = 7, B_DRAIN = 8, NBARS = 9;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;
   static constexpr uint32_t TOTAL = MISC_OFF + 16;
 };
@@ -125,8 +125,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Ly::B_QFULL), 1);
-    mbar_init(bar(Ly::B_KVFULL), 1);
-    mbar_init(bar(Ly::B_KVEMPTY), 1);
+    mbar_init(bar(Ly::B_KFULL), 1);
+    mbar_init(bar(Ly::B_KEMPTY), 1);
+    mbar_init(bar(Ly::B_VFULL), 1);
+    mbar_init(bar(Ly::B_VEMPTY), 1);
     mbar_init(bar(Ly::B_SFULL), 1);
     mbar_init(bar(Ly::B_PFULL), 4);  // one lane of each softmax warp
     mbar_init(bar(Ly::B_OFULL), 1);
@@ -261,7 +263,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = run && NB > 0;
     if (ok) ok = mbar_wait_warp(bar(Ly::B_QFULL), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, -1);
     for (int j = 0; j < NB && ok; ++j) {
-      ok = mbar_wait_warp(bar(Ly::B_KVFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA,
+      ok = mbar_wait_warp(bar(Ly::B_KFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA,
                           j);
       if (!ok) break;
       tc_fence_after();
@@ -274,7 +276,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_mma_ss_warp(tmem, qd + qoff(kk), kd + koff(kk), idesc_qk, (pr > 0 || kk > 0) ? 1u : 0u);
       }
       tc_commit_warp(bar(Ly::B_SFULL));
+      tc_commit_warp(bar(Ly::B_KEMPTY));  // K(j) free once S(j) completes: K(j+1) loads during softmax(j), PV(j)
       ok = mbar_wait_warp(bar(Ly::B_PFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
+      if (ok)
+        ok = mbar_wait_warp(bar(Ly::B_VFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA,
+                            j);
       if (!ok) break;
       tc_fence_after();
       // O += P V over the six piece pairs; P's pieces from TMEM, V's MN-major from shared memory
@@ -286,7 +292,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_mma_ts_warp(tmem + COL_O, pa + (uint32_t)(kk * 8), vd + (uint64_t)(kk * 128), idesc_pv,
                          (j > 0 || pr > 0 || kk > 0) ? 1u : 0u);
       }
-      tc_commit_warp(bar(Ly::B_KVEMPTY));  // K(j), V(j) free once these products complete
+      tc_commit_warp(bar(Ly::B_VEMPTY));  // V(j) free once these products complete: V(j+1) loads during S(j+1)
     }
     if (ok) tc_commit_warp(bar(Ly::B_OFULL));
     tc_commit_warp(bar(Ly::B_DRAIN));
@@ -294,7 +300,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == WARP_LOAD && lane == 0) {
     // ================================================================ producer
     bool ok = run && NB > 0;
-    int issued = 0;
+    int issued_k = 0, issued_v = 0;
     if (ok) {
       const int64_t qrow = ((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + (int64_t)qt * BM;
       mbar_expect_tx(bar(Ly::B_QFULL), 3 * Ly::QP);
@@ -304,12 +310,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                       (int32_t)(qrow + (int64_t)a * prm.q_rows), bar(Ly::B_QFULL));
     }
     const int64_t kvbase = ((int64_t)b * prm.Hkv + hk) * prm.S;
+    // K and V of a block have their own stages: K(j) is refilled as soon as S(j-1) is done with
+    // it (overlapping softmax(j-1) and PV(j-1)), V(j) once PV(j-1) is (overlapping S(j))
+    auto load_pieces = [&](const CUtensorMap* tm, uint32_t off, int64_t krow, int bfull) {
+      mbar_expect_tx(bar(bfull), 3 * Ly::KP);
+      for (int a = 0; a < 3; ++a)
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_2d(sb + off + (uint32_t)a * Ly::KP + (uint32_t)c * Ly::KBOX, tm, c * 64,
+                      (int32_t)(krow + (int64_t)a * prm.kv_rows), bar(bfull));
+    };
     for (int j = 0; j < NB && ok; ++j) {
-      if (j > 0) {
-        ok = mbar_wait(bar(Ly::B_KVEMPTY), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
-                       ROLE_LOAD, j);
-        if (!ok) break;
-      }
       int kp, kbk;
       block_at(j, kp, kbk);
       if (kp < 0 || kp >= prm.P) {
@@ -318,19 +328,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       const int64_t krow = kvbase + (int64_t)kp * L + (int64_t)kbk * BN;
-      mbar_expect_tx(bar(Ly::B_KVFULL), 6 * Ly::KP);
-      for (int a = 0; a < 3; ++a)
-        for (int c = 0; c < D / 64; ++c) {
-          const int32_t y = (int32_t)(krow + (int64_t)a * prm.kv_rows);
-          tma_load_2d(sb + Ly::K_OFF + (uint32_t)a * Ly::KP + (uint32_t)c * Ly::KBOX, &tmK, c * 64, y,
-                      bar(Ly::B_KVFULL));
-          tma_load_2d(sb + Ly::V_OFF + (uint32_t)a * Ly::KP + (uint32_t)c * Ly::KBOX, &tmV, c * 64, y,
-                      bar(Ly::B_KVFULL));
-        }
-      ++issued;
+      if (j > 0) {
+        ok = mbar_wait(bar(Ly::B_KEMPTY), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                       ROLE_LOAD, j);
+        if (!ok) break;
+      }
+      load_pieces(&tmK, Ly::K_OFF, krow, Ly::B_KFULL);
+      ++issued_k;
+      if (j > 0) {
+        ok = mbar_wait(bar(Ly::B_VEMPTY), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                       ROLE_LOAD, j);
+        if (!ok) break;
+      }
+      load_pieces(&tmV, Ly::V_OFF, krow, Ly::B_VFULL);
+      ++issued_v;
     }
     if (run && NB > 0) mbar_drain(bar(Ly::B_QFULL), 0u, DRAIN_NS);
-    if (issued > 0) mbar_drain(bar(Ly::B_KVFULL), (uint32_t)((issued - 1) & 1), DRAIN_NS);
+    if (issued_k > 0) mbar_drain(bar(Ly::B_KFULL), (uint32_t)((issued_k - 1) & 1), DRAIN_NS);
+    if (issued_v > 0) mbar_drain(bar(Ly::B_VFULL), (uint32_t)((issued_v - 1) & 1), DRAIN_NS);
   }
 
   tc_fence_before();
