@@ -15,10 +15,14 @@
 //   tile_fwd_tc32_kernel: one CTA per (work item, batch, head, 128-row query tile); 6 warps --
 //     warps 0-3 softmax (one thread per row = TMEM lane), warp 4 MMA issuer (elected lane of a
 //     converged warp), warp 5 TMA producer.  64-key blocks keep the three pieces of Q, K and V of
-//     a d = 128 block within shared memory (96 + 48 + 48 KB).  TMEM: S (64 columns; P's first and
-//     second pieces are written back as bf16 into them) | P's third piece (32) | O (d).  The row
-//     maximum is exact every block (no deferred reference), P is split into its three pieces in
-//     registers.
+//     a d = 128 block within shared memory (96 + 48 + 48 KB).  TMEM: S (64 columns) | P of even
+//     blocks (three packed bf16 pieces, 96 columns) | P of odd blocks (96) | O (d).  With P out of
+//     S's columns and double-buffered, S(j+1) is issued as soon as the softmax has read S(j) and
+//     before PV(j), so softmax(j+1) overlaps PV(j).  Products of one thread run in issue order:
+//     S(j) follows PV(j-2), so PV(j-2) is done with P's buffer when the softmax of block j
+//     refills it.  The softmax takes the block maximum every block but raises its reference (and
+//     rescales O and l) only when the maximum grew by more than 2^8; the exact three-piece split
+//     keeps P's full fp32 value at any magnitude up to that bound.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -66,7 +70,7 @@ struct Layout {
   static constexpr uint32_t Q_OFF = 0, K_OFF = 3 * QP, V_OFF = K_OFF + 3 * KP;
   static constexpr uint32_t BAR_OFF = V_OFF + 3 * KP;
   static constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 2, B_VFULL = 3, B_VEMPTY = 4, B_SFULL = 5, B_PFULL = 6,
-                       B_OFULL = 7, B_DRAIN = 8, NBARS = 9;
+                       B_OFULL = 7, B_DRAIN = 8, B_PVDONE = 9, NBARS = 10;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;
   static constexpr uint32_t TOTAL = MISC_OFF + 16;
 };
@@ -133,13 +137,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar(Ly::B_PFULL), 4);  // one lane of each softmax warp
     mbar_init(bar(Ly::B_OFULL), 1);
     mbar_init(bar(Ly::B_DRAIN), 1);
+    mbar_init(bar(Ly::B_PVDONE), 1);
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(prm.status) != 0 || !unit_ok) ? 1 : 0;
     if (!unit_ok) record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_ITEM, (int32_t)blockIdx.x);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == WARP_MMA) {
-    tmem_alloc(smem_u32(tmem_slot), 256);
+    tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
   if (warp == WARP_LOAD && lane == 0) {
@@ -152,16 +157,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool run = *abort_flag == 0;
-  // TMEM columns: S [0, 64) (P pieces 0 and 1 packed into [0, 32) and [32, 64)), P piece 2
-  // packed into [64, 96), O [128, 128 + D)
-  constexpr uint32_t COL_PL = 64, COL_O = 128;
+  // TMEM columns: S [0, 64); P of block j in [64 + 96 (j % 2), + 96) as three packed bf16 pieces
+  // of 32 columns; O [256, 256 + D)
+  constexpr uint32_t COL_P = 64, COL_O = 256;
+  constexpr float LOG2_RESCALE = 8.0f;
 
   if (warp < 4) {
     // ================================================================ softmax
     const int row = warp * 32 + lane;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const uint32_t tm_s = tmem + lane_base;
-    const uint32_t tm_pl = tmem + lane_base + COL_PL;
     const uint32_t tm_o = tmem + lane_base + COL_O;
     const int64_t q_local = (int64_t)qt * BM + row;
     float m = -INFINITY, l = 0.f;
@@ -186,12 +191,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         s[c] = (c < hi) ? s[c] * prm.scale_log2 : -INFINITY;
         mb = fmaxf(mb, s[c]);
       }
-      const float m_new = fmaxf(m, mb);
-      const float mref = (m_new == -INFINITY) ? 0.f : m_new;
-      const float factor = (m == -INFINITY) ? 1.f : exp2f(m - mref);
-      m = m_new;
-      if (__any_sync(0xffffffffu, factor != 1.f) && j > 0) {
-        // O holds every earlier PV product: S(j) was issued after PV(j-1)
+      // reference m: set by the first visible block, raised only when the maximum grows by more
+      // than 2^LOG2_RESCALE (then O and l are rescaled); P = 2^(s - m) <= 2^LOG2_RESCALE
+      float factor = 1.f;
+      if (mb > -INFINITY) {
+        if (m == -INFINITY) {
+          m = mb;
+        } else if (mb > m + LOG2_RESCALE) {
+          factor = fast_exp2(m - mb);
+          m = mb;
+        }
+      }
+      const float mref = (m == -INFINITY) ? 0.f : m;
+      if (__any_sync(0xffffffffu, factor != 1.f)) {
+        // O must hold every earlier PV product: wait for PV(j-1) (issued after S(j), so possibly
+        // still running; PV(j) needs this block's P, so the barrier is not a phase ahead)
+        ok = mbar_wait(bar(Ly::B_PVDONE), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                       ROLE_SOFTMAX, j);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           float o[32];
@@ -219,9 +238,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         p3[c / 2] = *reinterpret_cast<const uint32_t*>(&cc);
       }
       l = l * factor + sum;
-      tmem_st32(tm_s, p1);
-      tmem_st32(tm_s + 32u, p2);
-      tmem_st32(tm_pl, p3);
+      const uint32_t tm_p = tmem + lane_base + COL_P + 96u * (uint32_t)(j & 1);
+      tmem_st32(tm_p, p1);
+      tmem_st32(tm_p + 32u, p2);
+      tmem_st32(tm_p + 64u, p3);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -259,15 +279,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // K-major operand made of 64-column SW128 boxes: K-step kk sits in box kk/4 at byte 32 (kk % 4)
     auto qoff = [](int kk) { return (uint64_t)((kk >> 2) * (Ly::QBOX >> 4) + (kk & 3) * 2); };
     auto koff = [](int kk) { return (uint64_t)((kk >> 2) * (Ly::KBOX >> 4) + (kk & 3) * 2); };
-    const uint32_t p_col[3] = {0u, 32u, COL_PL};
     bool ok = run && NB > 0;
     if (ok) ok = mbar_wait_warp(bar(Ly::B_QFULL), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, -1);
-    for (int j = 0; j < NB && ok; ++j) {
-      ok = mbar_wait_warp(bar(Ly::B_KFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA,
-                          j);
-      if (!ok) break;
+    // S(j) = Q K(j)^T over the six piece pairs; K(j) is free once it completes
+    auto issue_s = [&](int j) -> bool {
+      if (!mbar_wait_warp(bar(Ly::B_KFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j))
+        return false;
       tc_fence_after();
-      // S = Q K^T over the six piece pairs
       for (int pr = 0; pr < NPAIR; ++pr) {
         const uint64_t qd = q0 + (uint64_t)pair_a(pr) * (Ly::QP >> 4);
         const uint64_t kd = k0 + (uint64_t)pair_b(pr) * (Ly::KP >> 4);
@@ -276,23 +294,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_mma_ss_warp(tmem, qd + qoff(kk), kd + koff(kk), idesc_qk, (pr > 0 || kk > 0) ? 1u : 0u);
       }
       tc_commit_warp(bar(Ly::B_SFULL));
-      tc_commit_warp(bar(Ly::B_KEMPTY));  // K(j) free once S(j) completes: K(j+1) loads during softmax(j), PV(j)
+      tc_commit_warp(bar(Ly::B_KEMPTY));
+      return true;
+    };
+    if (ok) ok = issue_s(0);
+    for (int j = 0; j < NB && ok; ++j) {
+      // the softmax has read S(j) and written P(j): S(j+1) may overwrite S and run while the
+      // softmax of block j+1 waits for it, ahead of PV(j)
       ok = mbar_wait_warp(bar(Ly::B_PFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
+      if (ok && j + 1 < NB) ok = issue_s(j + 1);
       if (ok)
         ok = mbar_wait_warp(bar(Ly::B_VFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA,
                             j);
       if (!ok) break;
       tc_fence_after();
-      // O += P V over the six piece pairs; P's pieces from TMEM, V's MN-major from shared memory
+      // O += P V over the six piece pairs; P's pieces from TMEM (buffer j % 2), V's MN-major from
+      // shared memory
+      const uint32_t pbuf = tmem + COL_P + 96u * (uint32_t)(j & 1);
       for (int pr = 0; pr < NPAIR; ++pr) {
-        const uint32_t pa = tmem + p_col[pair_a(pr)];
+        const uint32_t pa = pbuf + 32u * (uint32_t)pair_a(pr);
         const uint64_t vd = v0 + (uint64_t)pair_b(pr) * (Ly::KP >> 4);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           tc_mma_ts_warp(tmem + COL_O, pa + (uint32_t)(kk * 8), vd + (uint64_t)(kk * 128), idesc_pv,
                          (j > 0 || pr > 0 || kk > 0) ? 1u : 0u);
       }
-      tc_commit_warp(bar(Ly::B_VEMPTY));  // V(j) free once these products complete: V(j+1) loads during S(j+1)
+      tc_commit_warp(bar(Ly::B_VEMPTY));  // V(j) free once these products complete
+      tc_commit_warp(bar(Ly::B_PVDONE));  // O holds PV(0..j): a rescale of block j+1 may start
     }
     if (ok) tc_commit_warp(bar(Ly::B_OFULL));
     tc_commit_warp(bar(Ly::B_DRAIN));
@@ -310,8 +338,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                       (int32_t)(qrow + (int64_t)a * prm.q_rows), bar(Ly::B_QFULL));
     }
     const int64_t kvbase = ((int64_t)b * prm.Hkv + hk) * prm.S;
-    // K and V of a block have their own stages: K(j) is refilled as soon as S(j-1) is done with
-    // it (overlapping softmax(j-1) and PV(j-1)), V(j) once PV(j-1) is (overlapping S(j))
+    // K and V of a block have their own stages.  Products run S(j), PV(j-1), S(j+1), PV(j), ...,
+    // so K(j) (free when S(j-1) completes) is due before V(j-1) (free when PV(j-2) completes):
+    // loads go K(0), V(0), K(1), then K(j), V(j-1) for j >= 2, then the last V.
     auto load_pieces = [&](const CUtensorMap* tm, uint32_t off, int64_t krow, int bfull) {
       mbar_expect_tx(bar(bfull), 3 * Ly::KP);
       for (int a = 0; a < 3; ++a)
@@ -319,30 +348,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tma_load_2d(sb + off + (uint32_t)a * Ly::KP + (uint32_t)c * Ly::KBOX, tm, c * 64,
                       (int32_t)(krow + (int64_t)a * prm.kv_rows), bar(bfull));
     };
-    for (int j = 0; j < NB && ok; ++j) {
+    auto row_of = [&](int j, int64_t& krow) -> bool {
       int kp, kbk;
       block_at(j, kp, kbk);
       if (kp < 0 || kp >= prm.P) {
         record_error(prm.status, MESH_ATTN_ERR_OUT_OF_RANGE, ROLE_LOAD, (int32_t)blockIdx.x);
         *abort_flag = 1;
-        break;
+        return false;
       }
-      const int64_t krow = kvbase + (int64_t)kp * L + (int64_t)kbk * BN;
-      if (j > 0) {
-        ok = mbar_wait(bar(Ly::B_KEMPTY), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
-                       ROLE_LOAD, j);
-        if (!ok) break;
-      }
+      krow = kvbase + (int64_t)kp * L + (int64_t)kbk * BN;
+      return true;
+    };
+    auto load_k = [&](int j) -> bool {
+      int64_t krow;
+      if (!row_of(j, krow)) return false;
+      if (j > 0 && !mbar_wait(bar(Ly::B_KEMPTY), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                              ROLE_LOAD, j))
+        return false;
       load_pieces(&tmK, Ly::K_OFF, krow, Ly::B_KFULL);
       ++issued_k;
-      if (j > 0) {
-        ok = mbar_wait(bar(Ly::B_VEMPTY), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
-                       ROLE_LOAD, j);
-        if (!ok) break;
-      }
+      return true;
+    };
+    auto load_v = [&](int j) -> bool {
+      int64_t krow;
+      if (!row_of(j, krow)) return false;
+      if (j > 0 && !mbar_wait(bar(Ly::B_VEMPTY), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                              ROLE_LOAD, j))
+        return false;
       load_pieces(&tmV, Ly::V_OFF, krow, Ly::B_VFULL);
       ++issued_v;
+      return true;
+    };
+    if (ok) ok = load_k(0) && load_v(0);
+    for (int j = 1; j < NB && ok; ++j) {
+      ok = load_k(j);
+      if (ok && j >= 2) ok = load_v(j - 1);
     }
+    if (ok && NB >= 2) ok = load_v(NB - 1);
     if (run && NB > 0) mbar_drain(bar(Ly::B_QFULL), 0u, DRAIN_NS);
     if (issued_k > 0) mbar_drain(bar(Ly::B_KFULL), (uint32_t)((issued_k - 1) & 1), DRAIN_NS);
     if (issued_v > 0) mbar_drain(bar(Ly::B_VFULL), (uint32_t)((issued_v - 1) & 1), DRAIN_NS);
@@ -352,7 +394,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   if (warp == WARP_MMA) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
