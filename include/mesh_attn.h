@@ -130,6 +130,15 @@ int mesh_attn_plan_slots(const mesh_attn_plan* plan, int32_t* slot_off);
 int mesh_attn_plan_order(const mesh_attn_plan* plan, int32_t* items, int32_t* item_step,
                          int32_t* kv_off, int32_t* kv_list);
 
+/* The order in which the kernels take the work items: order[j] (n_slots int32, caller array) is
+ * the index, in mesh_attn_plan_order's list, of the j-th item the kernels take.  The greedy pass
+ * (tutorial §"贪心算法：寻找最优的'流水线'") fixes each virtual device's order of work; the
+ * public list interleaves the devices step by step.  One GPU takes the devices' sequences tile
+ * after tile (row-major over the mesh), each in its own greedy order, so that the work items
+ * running together share a tile's KV partitions and its mesh row's Q partitions in L2.  A ring
+ * plan is taken in its public order.  A permutation of 0 .. n_slots - 1. */
+int mesh_attn_plan_launch_order(const mesh_attn_plan* plan, int32_t* order);
+
 /* Receive volumes a real mesh would move, per device v (tutorial §"Mesh-Attention：从一维'环'
  * 到二维'网'": per-device traffic grows as O(sqrt(N)) rather than Ring's O(N); abstract: a
  * device gathers only some of the Q and KV partitions).

@@ -273,3 +273,27 @@ def test_workspace_size_for_fp32_pieces(lib):
     # an fp32 call with only the bf16-sized workspace is refused before anything is enqueued
     assert so.mesh_attn_tile_fwd(p.handle, 0, 1, 16, 4, 128, fake, fake, fake, 0.1, fake, fake, fake, base, fake,
                                  None) == 9
+
+
+@pytest.mark.parametrize("P", [1, 4, 16, 64, 256])
+@pytest.mark.parametrize("causal,kvr,greedy", list(itertools.product([0, 1], repeat=3)))
+def test_launch_order_keeps_each_device_sequence(lib, P, causal, kvr, greedy):
+    """The kernels take the work items tile after tile (row-major over the mesh), each tile's
+    items in that virtual device's order from the plan: a permutation of the plan's items whose
+    tiles never decrease and whose positions in the plan's order increase within a tile."""
+    S = 64 * P
+    plan = lib.mesh_attn_plan_create(S, P, causal, kvr, greedy)
+    items, steps, _ = lib.mesh_attn_plan_order(plan)
+    order = lib.mesh_attn_plan_launch_order(plan)
+    assert sorted(order) == list(range(len(items)))
+    tiles = [items[i][1] for i in order]
+    assert tiles == sorted(tiles)
+    for a, b in zip(order, order[1:]):
+        if items[a][1] == items[b][1]:
+            assert a < b and steps[a] <= steps[b]
+
+
+@pytest.mark.parametrize("P", [1, 5, 16])
+def test_launch_order_of_ring_plan_is_its_order(lib, P):
+    plan = lib.mesh_attn_plan_create_ring(32 * P, P, True)
+    assert lib.mesh_attn_plan_launch_order(plan) == list(range(P))

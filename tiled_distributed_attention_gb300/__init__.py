@@ -52,6 +52,7 @@ _SIGS = {
     "mesh_attn_plan_slots": (c_i32, [c_vp, P_i32]),
     "mesh_attn_plan_order": (c_i32, [c_vp, P_i32, P_i32, P_i32, P_i32]),
     "mesh_attn_plan_volumes": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, P_i32, P_i64, P_i64]),
+    "mesh_attn_plan_launch_order": (c_i32, [c_vp, P_i32]),
     "mesh_attn_partials_size": (c_i32, [c_vp, c_i32, c_i32, c_i32, P_sz, P_sz]),
     "mesh_attn_workspace_size": (c_i32, [c_vp, P_sz]),
     "mesh_attn_workspace_size_for": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, P_sz]),
@@ -192,6 +193,14 @@ def mesh_attn_plan_order(plan: Plan):
     kvl = list(kv_list[:plan.n_kv_entries])
     return ([tuple(items[3 * i:3 * i + 3]) for i in range(n)], list(steps[:n]),
             [kvl[off[i]:off[i + 1]] for i in range(n)])
+
+
+def mesh_attn_plan_launch_order(plan: Plan):
+    """Indices into mesh_attn_plan_order's item list, in the order the kernels take the items."""
+    n = plan.n_slots
+    out = (c_i32 * max(n, 1))()
+    _check(_lib.mesh_attn_plan_launch_order(plan.handle, out), "mesh_attn_plan_launch_order")
+    return [out[i] for i in range(n)]
 
 
 def mesh_attn_plan_volumes(plan: Plan, Hq: int, Hkv: int, d: int, dtype: torch.dtype = torch.bfloat16):

@@ -160,6 +160,15 @@ int mesh_attn_plan_order(const mesh_attn_plan* plan, int32_t* items, int32_t* it
   });
 }
 
+int mesh_attn_plan_launch_order(const mesh_attn_plan* plan, int32_t* order) {
+  return guarded([&] {
+    if (!plan) return fail(MESH_ATTN_ERR_INVALID_ARG, "plan is NULL");
+    const mesh::Plan& p = plan->p;
+    if (order && !p.launch.empty()) std::memcpy(order, p.launch.data(), p.launch.size() * sizeof(int32_t));
+    return (int)MESH_ATTN_OK;
+  });
+}
+
 int mesh_attn_plan_volumes(const mesh_attn_plan* plan, int32_t Hq, int32_t Hkv, int32_t d, mesh_attn_dtype dtype,
                            int32_t* counts, int64_t* bytes, int64_t* ring_bytes) {
   return guarded([&] {

@@ -34,7 +34,8 @@ struct Plan {
   std::vector<int32_t> kv_off;             // [n+1]
   std::vector<int32_t> kv_list;            // [kv_off[n]]
   std::vector<int32_t> recv;               // [P*3] Q, KV, partial-O partitions received
-  std::vector<DevItem> dev_items;          // [n] the kernels' copy of the order
+  std::vector<DevItem> dev_items;          // [n] the kernels' copy of the work list, in launch order
+  std::vector<int32_t> launch;             // [n] launch position -> index in `items`
   // Backward pass: the (KV partition k, tile t) pairs with a live block, grouped by k, tiles
   // ascending; each with the tile's Q partitions live for k, ascending.
   std::vector<int32_t> kv_slot_off;        // [P+1]

@@ -199,6 +199,7 @@ void build_plan(Plan& pl, int64_t S, int32_t P, bool causal, bool kvr, bool gree
     const Key& k = keys[launch[j]];
     pl.dev_items[j] = DevItem{k.p, k.slot, pl.kv_off[launch[j]], k.n_kv};
   }
+  pl.launch = std::move(launch);
   build_kv_slots(pl);
 }
 
@@ -260,6 +261,7 @@ void build_ring_plan(Plan& pl, int64_t S, int32_t P, bool causal) {
       if (live(v, k, causal)) { pl.kv_list.push_back(k); ++n; }
     }
     pl.dev_items[i] = DevItem{v, v, (int32_t)pos, n};
+    pl.launch.push_back(i);  // ring: the kernels take the items in the public order
     pos += n;
     pl.n_steps = std::max(pl.n_steps, order[i].first);
   }
