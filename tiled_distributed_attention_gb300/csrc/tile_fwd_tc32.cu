@@ -14,9 +14,12 @@
 //                 workspace (HBM-bound, one pass).
 //   tile_fwd_tc32_kernel: one CTA per (work item, batch, head, 128-row query tile); 6 warps --
 //     warps 0-3 softmax (one thread per row = TMEM lane), warp 4 MMA issuer (elected lane of a
-//     converged warp), warp 5 TMA producer.  64-key blocks keep the three pieces of Q, K and V of
-//     a d = 128 block within shared memory (96 + 48 + 48 KB).  TMEM: S (64 columns) | P of even
-//     blocks (three packed bf16 pieces, 96 columns) | P of odd blocks (96) | O (d).  With P out of
+//     converged warp), warp 5 TMA producer.  Q's first two pieces sit in TMEM, written there by
+//     the softmax warps at the start of the unit, and are the A operand of five of the six S
+//     products, which then read only K from shared memory; shared memory holds Q's third piece,
+//     two stages of K's three pieces and one of V's (32 + 96 + 48 KB at d = 128), 64 keys a
+//     block.  TMEM: S (64 columns) | P of even blocks (three packed bf16 pieces, 96 columns) | P
+//     of odd blocks (96) | O (d) | Q1, Q2 (d / 2 each, packed pairs).  With P out of
 //     S's columns and double-buffered, S(j+1) is issued as soon as the softmax has read S(j) and
 //     before PV(j), so softmax(j+1) overlaps PV(j).  Products of one thread run in issue order:
 //     S(j) follows PV(j-2), so PV(j-2) is done with P's buffer when the softmax of block j
@@ -56,6 +59,7 @@ struct Params {
   int32_t* status;
   int64_t S, L;
   int64_t q_rows, kv_rows;  // rows of one piece: B*Hq*S and B*Hkv*S
+  const uint32_t* q_pieces;  // Q's bf16 pieces [3][q_rows][D], as packed pairs
   int32_t B, Hq, Hkv, P, n_items, n_slots, nqt, nb, causal;
   float scale_log2;
   int64_t wait_limit_ns;
@@ -67,10 +71,12 @@ struct Layout {
   static constexpr uint32_t KP = BN * D * 2;    // one piece of a K or V block
   static constexpr uint32_t QBOX = BM * 128;    // 128 rows x 64 bf16 columns
   static constexpr uint32_t KBOX = BN * 128;    // 64 rows x 64 bf16 columns
-  static constexpr uint32_t Q_OFF = 0, K_OFF = 3 * QP, V_OFF = K_OFF + 3 * KP;
+  // Q's third piece (the first two live in TMEM), two K stages, one V stage
+  static constexpr uint32_t KSTAGE = 3 * KP;
+  static constexpr uint32_t Q_OFF = 0, K_OFF = QP, V_OFF = K_OFF + 2 * KSTAGE;
   static constexpr uint32_t BAR_OFF = V_OFF + 3 * KP;
-  static constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 2, B_VFULL = 3, B_VEMPTY = 4, B_SFULL = 5, B_PFULL = 6,
-                       B_OFULL = 7, B_DRAIN = 8, B_PVDONE = 9, NBARS = 10;
+  static constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 3, B_VFULL = 5, B_VEMPTY = 6, B_SFULL = 7, B_PFULL = 8,
+                       B_OFULL = 9, B_DRAIN = 10, B_PVDONE = 11, B_QTMEM = 12, NBARS = 13;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;
   static constexpr uint32_t TOTAL = MISC_OFF + 16;
 };
@@ -129,8 +135,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Ly::B_QFULL), 1);
-    mbar_init(bar(Ly::B_KFULL), 1);
-    mbar_init(bar(Ly::B_KEMPTY), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(Ly::B_KFULL + s), 1);
+      mbar_init(bar(Ly::B_KEMPTY + s), 1);
+    }
+    mbar_init(bar(Ly::B_QTMEM), 4);  // one lane of each softmax warp
     mbar_init(bar(Ly::B_VFULL), 1);
     mbar_init(bar(Ly::B_VEMPTY), 1);
     mbar_init(bar(Ly::B_SFULL), 1);
@@ -158,8 +167,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const bool run = *abort_flag == 0;
   // TMEM columns: S [0, 64); P of block j in [64 + 96 (j % 2), + 96) as three packed bf16 pieces
-  // of 32 columns; O [256, 256 + D)
-  constexpr uint32_t COL_P = 64, COL_O = 256;
+  // of 32 columns; O [256, 256 + D); Q's first and second pieces [256 + D, + D / 2) each, packed
+  // (the A operand of the S products that take them)
+  constexpr uint32_t COL_P = 64, COL_O = 256, COL_Q = COL_O + D, QW = D / 2;
   constexpr float LOG2_RESCALE = 8.0f;
 
   if (warp < 4) {
@@ -171,6 +181,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int64_t q_local = (int64_t)qt * BM + row;
     float m = -INFINITY, l = 0.f;
     bool ok = run;
+    if (ok) {
+      // this row's first two Q pieces into TMEM (lane = row): rows past the tensor read as zero
+      const int64_t grow = ((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + q_local;
+      const uint32_t tm_q = tmem + lane_base + COL_Q;
+#pragma unroll 1
+      for (int a = 0; a < 2; ++a) {
+        uint32_t w[QW];
+        if (grow < prm.q_rows) {
+          const uint4* src = reinterpret_cast<const uint4*>(prm.q_pieces + ((int64_t)a * prm.q_rows + grow) * QW);
+#pragma unroll
+          for (int i = 0; i < QW / 4; ++i) {
+            const uint4 v = __ldg(src + i);
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < QW; ++i) w[i] = 0u;
+        }
+#pragma unroll
+        for (int c = 0; c < QW; c += 32) tmem_st32(tm_q + (uint32_t)(a * QW + c), w + c);
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Ly::B_QTMEM));
+    }
     for (int j = 0; j < NB && ok; ++j) {
       int kp, kbk;
       block_at(j, kp, kbk);
@@ -281,20 +320,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto koff = [](int kk) { return (uint64_t)((kk >> 2) * (Ly::KBOX >> 4) + (kk & 3) * 2); };
     bool ok = run && NB > 0;
     if (ok) ok = mbar_wait_warp(bar(Ly::B_QFULL), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, -1);
-    // S(j) = Q K(j)^T over the six piece pairs; K(j) is free once it completes
+    if (ok) ok = mbar_wait_warp(bar(Ly::B_QTMEM), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, -1);
+    // S(j) = Q K(j)^T over the six piece pairs: Q's first two pieces from TMEM (the products read
+    // only K from shared memory), its third from shared memory; K(j)'s stage is free once they
+    // complete
     auto issue_s = [&](int j) -> bool {
-      if (!mbar_wait_warp(bar(Ly::B_KFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j))
+      const int ks = j & 1;
+      if (!mbar_wait_warp(bar(Ly::B_KFULL + ks), (uint32_t)((j >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                          ROLE_MMA, j))
         return false;
       tc_fence_after();
       for (int pr = 0; pr < NPAIR; ++pr) {
-        const uint64_t qd = q0 + (uint64_t)pair_a(pr) * (Ly::QP >> 4);
-        const uint64_t kd = k0 + (uint64_t)pair_b(pr) * (Ly::KP >> 4);
+        const int pa = pair_a(pr);
+        const uint64_t kd = k0 + (uint64_t)ks * (Ly::KSTAGE >> 4) + (uint64_t)pair_b(pr) * (Ly::KP >> 4);
+        if (pa < 2) {
+          const uint32_t qa = tmem + COL_Q + (uint32_t)(pa * QW);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc_mma_ss_warp(tmem, qd + qoff(kk), kd + koff(kk), idesc_qk, (pr > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma_ts_warp(tmem, qa + (uint32_t)(kk * 8), kd + koff(kk), idesc_qk, (pr > 0 || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma_ss_warp(tmem, q0 + qoff(kk), kd + koff(kk), idesc_qk, (pr > 0 || kk > 0) ? 1u : 0u);
+        }
       }
       tc_commit_warp(bar(Ly::B_SFULL));
-      tc_commit_warp(bar(Ly::B_KEMPTY));
+      tc_commit_warp(bar(Ly::B_KEMPTY + ks));
       return true;
     };
     if (ok) ok = issue_s(0);
@@ -331,22 +382,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int issued_k = 0, issued_v = 0;
     if (ok) {
       const int64_t qrow = ((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + (int64_t)qt * BM;
-      mbar_expect_tx(bar(Ly::B_QFULL), 3 * Ly::QP);
-      for (int a = 0; a < 3; ++a)
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_2d(sb + Ly::Q_OFF + (uint32_t)a * Ly::QP + (uint32_t)c * Ly::QBOX, &tmQ, c * 64,
-                      (int32_t)(qrow + (int64_t)a * prm.q_rows), bar(Ly::B_QFULL));
+      mbar_expect_tx(bar(Ly::B_QFULL), Ly::QP);  // the third piece; the softmax warps put the others in TMEM
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_2d(sb + Ly::Q_OFF + (uint32_t)c * Ly::QBOX, &tmQ, c * 64, (int32_t)(qrow + 2 * prm.q_rows),
+                    bar(Ly::B_QFULL));
     }
     const int64_t kvbase = ((int64_t)b * prm.Hkv + hk) * prm.S;
-    // K and V of a block have their own stages.  Products run S(j), PV(j-1), S(j+1), PV(j), ...,
-    // so K(j) (free when S(j-1) completes) is due before V(j-1) (free when PV(j-2) completes):
-    // loads go K(0), V(0), K(1), then K(j), V(j-1) for j >= 2, then the last V.
-    auto load_pieces = [&](const CUtensorMap* tm, uint32_t off, int64_t krow, int bfull) {
-      mbar_expect_tx(bar(bfull), 3 * Ly::KP);
+    // Two K stages and one V stage.  Products run S(j), PV(j-1), S(j+1), PV(j), ...; K(j) takes the
+    // stage S(j-2) frees, V(j) the one PV(j-1) frees: loads go K(0), K(1), V(0), then K(j), V(j-1)
+    // for j >= 2, then the last V.
+    auto load_pieces = [&](const CUtensorMap* tm, uint32_t off, int64_t krow, uint32_t fullbar) {
+      mbar_expect_tx(fullbar, 3 * Ly::KP);
       for (int a = 0; a < 3; ++a)
         for (int c = 0; c < D / 64; ++c)
           tma_load_2d(sb + off + (uint32_t)a * Ly::KP + (uint32_t)c * Ly::KBOX, tm, c * 64,
-                      (int32_t)(krow + (int64_t)a * prm.kv_rows), bar(bfull));
+                      (int32_t)(krow + (int64_t)a * prm.kv_rows), fullbar);
     };
     auto row_of = [&](int j, int64_t& krow) -> bool {
       int kp, kbk;
@@ -362,10 +412,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto load_k = [&](int j) -> bool {
       int64_t krow;
       if (!row_of(j, krow)) return false;
-      if (j > 0 && !mbar_wait(bar(Ly::B_KEMPTY), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
-                              ROLE_LOAD, j))
+      const int ks = j & 1;
+      if (j >= 2 && !mbar_wait(bar(Ly::B_KEMPTY + ks), (uint32_t)(((j - 2) >> 1) & 1), prm.wait_limit_ns, abort_flag,
+                               prm.status, ROLE_LOAD, j))
         return false;
-      load_pieces(&tmK, Ly::K_OFF, krow, Ly::B_KFULL);
+      load_pieces(&tmK, Ly::K_OFF + (uint32_t)ks * Ly::KSTAGE, krow, bar(Ly::B_KFULL + ks));
       ++issued_k;
       return true;
     };
@@ -375,18 +426,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (j > 0 && !mbar_wait(bar(Ly::B_VEMPTY), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
                               ROLE_LOAD, j))
         return false;
-      load_pieces(&tmV, Ly::V_OFF, krow, Ly::B_VFULL);
+      load_pieces(&tmV, Ly::V_OFF, krow, bar(Ly::B_VFULL));
       ++issued_v;
       return true;
     };
-    if (ok) ok = load_k(0) && load_v(0);
-    for (int j = 1; j < NB && ok; ++j) {
+    if (ok) ok = load_k(0);
+    if (ok && NB > 1) ok = load_k(1);
+    if (ok) ok = load_v(0);
+    for (int j = 2; j < NB && ok; ++j) {
       ok = load_k(j);
-      if (ok && j >= 2) ok = load_v(j - 1);
+      if (ok) ok = load_v(j - 1);
     }
     if (ok && NB >= 2) ok = load_v(NB - 1);
     if (run && NB > 0) mbar_drain(bar(Ly::B_QFULL), 0u, DRAIN_NS);
-    if (issued_k > 0) mbar_drain(bar(Ly::B_KFULL), (uint32_t)((issued_k - 1) & 1), DRAIN_NS);
+    for (int jj = (issued_k > 2 ? issued_k - 2 : 0); jj < issued_k; ++jj)
+      mbar_drain(bar(Ly::B_KFULL + (jj & 1)), (uint32_t)((jj >> 1) & 1), DRAIN_NS);
     if (issued_v > 0) mbar_drain(bar(Ly::B_VFULL), (uint32_t)((issued_v - 1) & 1), DRAIN_NS);
   }
 
@@ -508,6 +562,7 @@ static int launch(const TileArgs& a, void* stream, std::string* err) {
   prm.L = a.L;
   prm.q_rows = q_rows;
   prm.kv_rows = kv_rows;
+  prm.q_pieces = reinterpret_cast<const uint32_t*>(base + pc.q_off);
   prm.B = a.B;
   prm.Hq = a.Hq;
   prm.Hkv = a.Hkv;
