@@ -1,10 +1,14 @@
 // Tile attention forward for fp32 inputs on the 5th-generation tensor cores (sm_103a), with fp32
 // accuracy: every fp32 operand x is split exactly into three bf16 pieces x = x1 + x2 + x3
-// (8 + 8 + 8 significant bits: x1 = bf16(x), x2 = bf16(x - x1), x3 = bf16(x - x1 - x2)), and a
-// product sums the six piece products whose order is at least 2^-16 of the whole,
+// (8 + 8 + 8 significant bits), and a product sums the six piece products whose order is at
+// least 2^-16 of the whole,
 //   x1 y1 + x1 y2 + x2 y1 + x1 y3 + x3 y1 + x2 y2,
-// on bf16 tensor-core products with fp32 accumulation; the terms left out are O(2^-24).  Six
-// bf16 products cost what three tf32 products cost.
+// on bf16 tensor-core products with fp32 accumulation.  Q, K and V are split by rounding to
+// nearest (x1 = bf16(x), x2 = bf16(x - x1), x3 = bf16(x - x1 - x2): |x2| <= 2^-8 |x|,
+// |x3| <= 2^-16 |x|), so the terms left out of Q K^T are below 2^-23 of |q||k|.  The
+// probabilities P are split in the softmax by truncation, which takes integer masks and byte
+// permutes instead of conversions (|p2| < 2^-7 p, |p3| < 2^-15 p), so the terms left out of
+// P V are below 2^-22 of p |v|.  Six bf16 products cost what three tf32 products cost.
 //
 // Same work decomposition and outputs as the bf16 kernel (Mesh-Attention tiles and partial
 // outputs: "Mesh-Attention: A New Communication-Efficient Distributed Attention with Improved
@@ -265,16 +269,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t p1[BN / 2], p2[BN / 2], p3[BN / 2];
 #pragma unroll
       for (int c = 0; c < BN; c += 2) {
-        const float e0 = exp2f(s[c] - mref), e1 = exp2f(s[c + 1] - mref);
+        const float e0 = fast_exp2(s[c] - mref), e1 = fast_exp2(s[c + 1] - mref);
         sum += e0 + e1;
-        // exact three-piece split of each probability
-        const __nv_bfloat162 a = __floats2bfloat162_rn(e0, e1);
-        const float r0 = e0 - __low2float(a), r1 = e1 - __high2float(a);
-        const __nv_bfloat162 bb = __floats2bfloat162_rn(r0, r1);
-        const __nv_bfloat162 cc = __floats2bfloat162_rn(r0 - __low2float(bb), r1 - __high2float(bb));
-        p1[c / 2] = *reinterpret_cast<const uint32_t*>(&a);
-        p2[c / 2] = *reinterpret_cast<const uint32_t*>(&bb);
-        p3[c / 2] = *reinterpret_cast<const uint32_t*>(&cc);
+        // exact three-piece split of each probability by truncation: x1 = x with the low 16 bits
+        // cleared (its top 8 significant bits), r = x - x1 (exact, at most 16 significant bits),
+        // x2 = r truncated the same way, x3 = r - x2 (at most 8 significant bits, so a bf16); each
+        // piece is the high half of an fp32 whose low half is zero
+        const uint32_t u0 = __float_as_uint(e0), u1 = __float_as_uint(e1);
+        const float r0 = e0 - __uint_as_float(u0 & 0xffff0000u), r1 = e1 - __uint_as_float(u1 & 0xffff0000u);
+        const uint32_t w0 = __float_as_uint(r0), w1 = __float_as_uint(r1);
+        const float t0 = r0 - __uint_as_float(w0 & 0xffff0000u), t1 = r1 - __uint_as_float(w1 & 0xffff0000u);
+        p1[c / 2] = __byte_perm(u0, u1, 0x7632u);
+        p2[c / 2] = __byte_perm(w0, w1, 0x7632u);
+        p3[c / 2] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x7632u);
       }
       l = l * factor + sum;
       const uint32_t tm_p = tmem + lane_base + COL_P + 96u * (uint32_t)(j & 1);
