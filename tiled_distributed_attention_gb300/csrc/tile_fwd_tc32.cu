@@ -22,14 +22,14 @@
 //     the softmax warps at the start of the unit, and are the A operand of five of the six S
 //     products, which then read only K from shared memory; shared memory holds Q's third piece,
 //     two stages of K's three pieces and one of V's (32 + 96 + 48 KB at d = 128), 64 keys a
-//     block.  TMEM: S (64 columns) | P of even blocks (three packed bf16 pieces, 96 columns) | P
-//     of odd blocks (96) | O (d) | Q1, Q2 (d / 2 each, packed pairs).  With P out of
-//     S's columns and double-buffered, S(j+1) is issued as soon as the softmax has read S(j) and
-//     before PV(j), so softmax(j+1) overlaps PV(j).  Products of one thread run in issue order:
-//     S(j) follows PV(j-2), so PV(j-2) is done with P's buffer when the softmax of block j
-//     refills it.  The softmax takes the block maximum every block but raises its reference (and
-//     rescales O and l) only when the maximum grew by more than 2^8; the exact three-piece split
-//     keeps P's full fp32 value at any magnitude up to that bound.
+//     block.  TMEM: S of even blocks (64 columns) | S of odd blocks (64) | P (three packed bf16
+//     pieces, 96) | O (d) | Q1, Q2 (d / 2 each, packed pairs).  Issue order S(0), S(1), then per
+//     block PV(j), S(j+2): with S double-buffered and P in its own columns, the S products of the
+//     next block run while the softmax works on this one, so the tensor pipe does not wait for
+//     the softmax between S and PV.  The softmax stores P(j) once PV(j-1) has completed.  It
+//     takes the block maximum every block but raises its reference (and rescales O and l) only
+//     when the maximum grew by more than 2^8; the exact three-piece split keeps P's full fp32
+//     value at any magnitude up to that bound.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -79,8 +79,8 @@ struct Layout {
   static constexpr uint32_t KSTAGE = 3 * KP;
   static constexpr uint32_t Q_OFF = 0, K_OFF = QP, V_OFF = K_OFF + 2 * KSTAGE;
   static constexpr uint32_t BAR_OFF = V_OFF + 3 * KP;
-  static constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 3, B_VFULL = 5, B_VEMPTY = 6, B_SFULL = 7, B_PFULL = 8,
-                       B_OFULL = 9, B_DRAIN = 10, B_PVDONE = 11, B_QTMEM = 12, NBARS = 13;
+  static constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 3, B_VFULL = 5, B_VEMPTY = 6, B_SFULL = 7, B_PFULL = 9,
+                       B_OFULL = 10, B_DRAIN = 11, B_PVDONE = 12, B_QTMEM = 13, NBARS = 14;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;
   static constexpr uint32_t TOTAL = MISC_OFF + 16;
 };
@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar(Ly::B_QTMEM), 4);  // one lane of each softmax warp
     mbar_init(bar(Ly::B_VFULL), 1);
     mbar_init(bar(Ly::B_VEMPTY), 1);
-    mbar_init(bar(Ly::B_SFULL), 1);
+    mbar_init(bar(Ly::B_SFULL), 1);  // one per S buffer
+    mbar_init(bar(Ly::B_SFULL + 1), 1);
     mbar_init(bar(Ly::B_PFULL), 4);  // one lane of each softmax warp
     mbar_init(bar(Ly::B_OFULL), 1);
     mbar_init(bar(Ly::B_DRAIN), 1);
@@ -170,10 +171,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const bool run = *abort_flag == 0;
-  // TMEM columns: S [0, 64); P of block j in [64 + 96 (j % 2), + 96) as three packed bf16 pieces
-  // of 32 columns; O [256, 256 + D); Q's first and second pieces [256 + D, + D / 2) each, packed
-  // (the A operand of the S products that take them)
-  constexpr uint32_t COL_P = 64, COL_O = 256, COL_Q = COL_O + D, QW = D / 2;
+  // TMEM columns: S of block j in [64 (j % 2), + 64); P [128, 224) as three packed bf16 pieces of
+  // 32 columns; O [256, 256 + D); Q's first and second pieces [256 + D, + D / 2) each, packed (the
+  // A operand of the S products that take them)
+  constexpr uint32_t COL_P = 128, COL_O = 256, COL_Q = COL_O + D, QW = D / 2;
   constexpr float LOG2_RESCALE = 8.0f;
 
   if (warp < 4) {
@@ -220,13 +221,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // visible keys of this row in the block: [0, hi)
       int hi = (int)min((int64_t)BN, L - (int64_t)kbk * BN);
       if (prm.causal && kp == p) hi = (int)min((int64_t)hi, q_local - (int64_t)kbk * BN + 1);
-      ok = mbar_wait(bar(Ly::B_SFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_SOFTMAX, j);
+      ok = mbar_wait(bar(Ly::B_SFULL + (j & 1)), (uint32_t)((j >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                     ROLE_SOFTMAX, j);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       float s[BN];
-      tmem_ld32(tm_s, s);
-      tmem_ld32(tm_s + 32u, s + 32);
+      tmem_ld32(tm_s + 64u * (uint32_t)(j & 1), s);
+      tmem_ld32(tm_s + 64u * (uint32_t)(j & 1) + 32u, s + 32);
       tc_wait_ld();
       float mb = -INFINITY;
 #pragma unroll
@@ -246,13 +248,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       const float mref = (m == -INFINITY) ? 0.f : m;
+      // PV(j-1) done: O holds every earlier product and P's buffer is free (PV(j) needs this
+      // block's P, so the barrier is never a phase ahead of this wait)
+      bool pv_done = (j == 0);
       if (__any_sync(0xffffffffu, factor != 1.f)) {
-        // O must hold every earlier PV product: wait for PV(j-1) (issued after S(j), so possibly
-        // still running; PV(j) needs this block's P, so the barrier is not a phase ahead)
         ok = mbar_wait(bar(Ly::B_PVDONE), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
                        ROLE_SOFTMAX, j);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
+        pv_done = true;
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
@@ -284,7 +288,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         p3[c / 2] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x7632u);
       }
       l = l * factor + sum;
-      const uint32_t tm_p = tmem + lane_base + COL_P + 96u * (uint32_t)(j & 1);
+      if (!pv_done) {
+        ok = mbar_wait(bar(Ly::B_PVDONE), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
+                       ROLE_SOFTMAX, j);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      const uint32_t tm_p = tmem + lane_base + COL_P;
       tmem_st32(tm_p, p1);
       tmem_st32(tm_p + 32u, p2);
       tmem_st32(tm_p + 64u, p3);
@@ -328,11 +339,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = run && NB > 0;
     if (ok) ok = mbar_wait_warp(bar(Ly::B_QFULL), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, -1);
     if (ok) ok = mbar_wait_warp(bar(Ly::B_QTMEM), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, -1);
-    // S(j) = Q K(j)^T over the six piece pairs: Q's first two pieces from TMEM (the products read
-    // only K from shared memory), its third from shared memory; K(j)'s stage is free once they
-    // complete
+    // S(j) = Q K(j)^T over the six piece pairs into S buffer j % 2: Q's first two pieces from TMEM
+    // (the products read only K from shared memory), its third from shared memory; K(j)'s stage
+    // is free once they complete
     auto issue_s = [&](int j) -> bool {
       const int ks = j & 1;
+      const uint32_t sd = tmem + 64u * (uint32_t)ks;
       if (!mbar_wait_warp(bar(Ly::B_KFULL + ks), (uint32_t)((j >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
                           ROLE_MMA, j))
         return false;
@@ -344,31 +356,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t qa = tmem + COL_Q + (uint32_t)(pa * QW);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            tc_mma_ts_warp(tmem, qa + (uint32_t)(kk * 8), kd + koff(kk), idesc_qk, (pr > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_ts_warp(sd, qa + (uint32_t)(kk * 8), kd + koff(kk), idesc_qk, (pr > 0 || kk > 0) ? 1u : 0u);
         } else {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            tc_mma_ss_warp(tmem, q0 + qoff(kk), kd + koff(kk), idesc_qk, (pr > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_ss_warp(sd, q0 + qoff(kk), kd + koff(kk), idesc_qk, (pr > 0 || kk > 0) ? 1u : 0u);
         }
       }
-      tc_commit_warp(bar(Ly::B_SFULL));
+      tc_commit_warp(bar(Ly::B_SFULL + ks));
       tc_commit_warp(bar(Ly::B_KEMPTY + ks));
       return true;
     };
+    // Issue order S(0), S(1), then per block PV(j), S(j+2): S(j+1) is computed while the softmax
+    // works on block j, and S(j+2) while it works on block j+1.
     if (ok) ok = issue_s(0);
+    if (ok && NB > 1) ok = issue_s(1);
     for (int j = 0; j < NB && ok; ++j) {
-      // the softmax has read S(j) and written P(j): S(j+1) may overwrite S and run while the
-      // softmax of block j+1 waits for it, ahead of PV(j)
       ok = mbar_wait_warp(bar(Ly::B_PFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
-      if (ok && j + 1 < NB) ok = issue_s(j + 1);
       if (ok)
         ok = mbar_wait_warp(bar(Ly::B_VFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA,
                             j);
       if (!ok) break;
       tc_fence_after();
-      // O += P V over the six piece pairs; P's pieces from TMEM (buffer j % 2), V's MN-major from
-      // shared memory
-      const uint32_t pbuf = tmem + COL_P + 96u * (uint32_t)(j & 1);
+      // O += P V over the six piece pairs; P's pieces from TMEM, V's MN-major from shared memory
+      const uint32_t pbuf = tmem + COL_P;
       for (int pr = 0; pr < NPAIR; ++pr) {
         const uint32_t pa = pbuf + 32u * (uint32_t)pair_a(pr);
         const uint64_t vd = v0 + (uint64_t)pair_b(pr) * (Ly::KP >> 4);
@@ -378,7 +389,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                          (j > 0 || pr > 0 || kk > 0) ? 1u : 0u);
       }
       tc_commit_warp(bar(Ly::B_VEMPTY));  // V(j) free once these products complete
-      tc_commit_warp(bar(Ly::B_PVDONE));  // O holds PV(0..j): a rescale of block j+1 may start
+      tc_commit_warp(bar(Ly::B_PVDONE));  // O holds PV(0..j) and P is free for block j+1
+      // the softmax read S(j) before it wrote P(j), so S(j+2) may overwrite S buffer j % 2
+      if (j + 2 < NB) ok = issue_s(j + 2);
     }
     if (ok) tc_commit_warp(bar(Ly::B_OFULL));
     tc_commit_warp(bar(Ly::B_DRAIN));
