@@ -415,6 +415,8 @@ def main():
     ap.add_argument("--workload", default="stress_256k", choices=sorted(WORKLOADS))
     ap.add_argument("--backward-workload", default="bf16_causal_16k", choices=sorted(WORKLOADS),
                     help="workload of the backward-pass object of the line")
+    ap.add_argument("--in-dtype", default=None, choices=["bf16", "f32"],
+                    help="override the workload's input dtype (f32 runs the three-piece tensor-core path)")
     ap.add_argument("--plan", default="mesh", choices=["mesh", "ring"],
                     help="tile assignment: sqrt(P) x sqrt(P) mesh with KVR (default) or Ring-Attention rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -425,6 +427,8 @@ def main():
                          "whose replay passes can slow a kernel by orders of magnitude")
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
+    if args.in_dtype is not None and args.in_dtype != w.dtype:
+        w = w.with_(dtype=args.in_dtype, name=f"{w.name}_{args.in_dtype}")
     if args.impl == "reference":
         return run_reference(args, w)
 
