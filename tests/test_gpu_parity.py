@@ -126,6 +126,25 @@ def test_full_size_sampled_rows(lib, name):
             assert torch.equal(O[0, h, 0].cpu(), v[0, h // g, 0])
 
 
+@pytest.mark.parametrize("name", ["bf16_causal_16k", "gqa_causal_64k"])
+def test_full_size_f32_sampled_rows(lib, name):
+    """The fp32 tensor-core path (three-piece split, six products, two S buffers) at full size:
+    the 16K causal and 64K GQA causal shapes with fp32 inputs, on 4096 sampled query rows per
+    head at the fp32 tolerance.  A unit here runs up to 128 key blocks of 64 keys (a 1,024-row
+    partition against up to 8 KV partitions), so the block pipeline, the K/V stage rings and the
+    running-maximum rescale all go round many times."""
+    w = WORKLOADS[name]
+    w = w.with_(dtype="f32", name=w.name + "_f32")
+    q, k, v = make_qkv(w)
+    O, LSE, po, pl, plan = run_gpu(lib, w, q, k, v)
+    del po, pl
+    check_sampled(w, O, LSE, q, k, v, sample_rows(w))
+    # causal row 0 sees key 0 alone: O = V[0] up to the fp32 accumulation of its three pieces
+    g = w.Hq // w.Hkv
+    for h in range(w.Hq):
+        assert torch.allclose(O[0, h, 0].cpu(), v[0, h // g, 0], rtol=0, atol=1e-6)
+
+
 @pytest.mark.parametrize("name", ["tiny_f32", "bf16_L128_causal", "bf16_ragged_L200", "bf16_gqa4_L1024_causal"])
 def test_ring_plan_through_kernels(lib, name):
     """Ring-Attention's row assignment (one slot per Q partition holding every live KV partition)
