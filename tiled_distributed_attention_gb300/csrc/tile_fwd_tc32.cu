@@ -16,9 +16,10 @@
 // "环形注意力：突破长序列处理瓶颈的分布式计算范式", §"数值稳定性：Log-Sum-Exp技术的分布式应用").
 //   split_kernel: Q, K and V into their bf16 pieces, [3][rows][d] each, in the caller's
 //                 workspace (HBM-bound, one pass).
-//   tile_fwd_tc32_kernel: one CTA per (work item, batch, head, 128-row query tile); 6 warps --
-//     warps 0-3 softmax (one thread per row = TMEM lane), warp 4 MMA issuer (elected lane of a
-//     converged warp), warp 5 TMA producer.  Q's first two pieces sit in TMEM, written there by
+//   tile_fwd_tc32_kernel: one CTA per (work item, batch, head, 128-row query tile); 10 warps --
+//     warps 0-7 softmax (two per TMEM lane quadrant: one thread per row, each warp 32 of a
+//     block's 64 keys, the pair swapping half-row maxima through shared memory and a bounded
+//     mbarrier), warp 8 MMA issuer (elected lane of a converged warp), warp 9 TMA producer.  Q's first two pieces sit in TMEM, written there by
 //     the softmax warps at the start of the unit, and are the A operand of five of the six S
 //     products, which then read only K from shared memory; shared memory holds Q's third piece,
 //     two stages of K's three pieces and one of V's (32 + 96 + 48 KB at d = 128), 64 keys a
@@ -44,9 +45,10 @@ namespace tc32 {
 
 constexpr int BM = 128;  // query rows per tile = TMEM lanes
 constexpr int BN = 64;   // keys per block
-constexpr int NUM_THREADS = 192;
-constexpr int WARP_MMA = 4;
-constexpr int WARP_LOAD = 5;
+constexpr int NUM_THREADS = 320;
+constexpr int N_SOFTMAX_WARPS = 8;  // two per TMEM lane quadrant, 32 of a block's 64 keys each
+constexpr int WARP_MMA = 8;
+constexpr int WARP_LOAD = 9;
 constexpr int NPAIR = 6;
 constexpr int64_t DRAIN_NS = 200000000;
 constexpr int ROLE_SOFTMAX = 1, ROLE_MMA = 2, ROLE_LOAD = 3, ROLE_ITEM = 4;
@@ -69,6 +71,16 @@ struct Params {
   int64_t wait_limit_ns;
 };
 
+// 32 lanes x 16 consecutive 32-bit columns: thread i of the warp writes lane (base + i).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 template <int D>
 struct Layout {
   static constexpr uint32_t QP = BM * D * 2;    // one piece of the Q tile
@@ -80,9 +92,12 @@ struct Layout {
   static constexpr uint32_t Q_OFF = 0, K_OFF = QP, V_OFF = K_OFF + 2 * KSTAGE;
   static constexpr uint32_t BAR_OFF = V_OFF + 3 * KP;
   static constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 3, B_VFULL = 5, B_VEMPTY = 6, B_SFULL = 7, B_PFULL = 9,
-                       B_OFULL = 10, B_DRAIN = 11, B_PVDONE = 12, B_QTMEM = 13, NBARS = 14;
+                       B_OFULL = 10, B_DRAIN = 11, B_PVDONE = 12, B_QTMEM = 13, B_XCH = 14, NBARS = 18;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;
-  static constexpr uint32_t TOTAL = MISC_OFF + 16;
+  // the two softmax warps of a lane quadrant swap their half-row maxima (and at the end their
+  // sums) here: [quadrant 4][phase parity 2][half 2][32 rows] floats
+  static constexpr uint32_t XCH_OFF = MISC_OFF + 16;
+  static constexpr uint32_t TOTAL = XCH_OFF + 4 * 2 * 2 * 32 * 4;
 };
 
 // 64-key blocks of KV partition k seen by query tile qt of partition p: on the causal diagonal
@@ -143,12 +158,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(Ly::B_KFULL + s), 1);
       mbar_init(bar(Ly::B_KEMPTY + s), 1);
     }
-    mbar_init(bar(Ly::B_QTMEM), 4);  // one lane of each softmax warp
+    mbar_init(bar(Ly::B_QTMEM), N_SOFTMAX_WARPS);  // one lane of each softmax warp
+    for (int q = 0; q < 4; ++q) mbar_init(bar(Ly::B_XCH + q), 2);  // the quadrant's two warps
     mbar_init(bar(Ly::B_VFULL), 1);
     mbar_init(bar(Ly::B_VEMPTY), 1);
     mbar_init(bar(Ly::B_SFULL), 1);  // one per S buffer
     mbar_init(bar(Ly::B_SFULL + 1), 1);
-    mbar_init(bar(Ly::B_PFULL), 4);  // one lane of each softmax warp
+    mbar_init(bar(Ly::B_PFULL), N_SOFTMAX_WARPS);  // one lane of each softmax warp
     mbar_init(bar(Ly::B_OFULL), 1);
     mbar_init(bar(Ly::B_DRAIN), 1);
     mbar_init(bar(Ly::B_PVDONE), 1);
@@ -177,39 +193,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr uint32_t COL_P = 128, COL_O = 256, COL_Q = COL_O + D, QW = D / 2;
   constexpr float LOG2_RESCALE = 8.0f;
 
-  if (warp < 4) {
+  if (warp < N_SOFTMAX_WARPS) {
     // ================================================================ softmax
-    const int row = warp * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t tm_s = tmem + lane_base;
-    const uint32_t tm_o = tmem + lane_base + COL_O;
+    // Warp w owns TMEM lane quadrant w % 4 (rows 32 (w % 4) ..) and half w / 4 of each block's 64
+    // keys (and of O's columns).  The two warps of a quadrant swap their half-row maxima every
+    // block, so they take the same reference m and the same rescale decisions; each keeps the
+    // sum of its half, added together at the end.
+    const int q4 = warp & 3, hf = warp >> 2;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const uint32_t tm_s = tmem + lane_base + 32u * (uint32_t)hf;
+    const uint32_t tm_o = tmem + lane_base + COL_O + (uint32_t)(hf * (D / 2));
+    volatile float* xch = reinterpret_cast<volatile float*>(smem + Ly::XCH_OFF) + q4 * 128;
+    const uint32_t xbar = bar(Ly::B_XCH + q4);
     const int64_t q_local = (int64_t)qt * BM + row;
     float m = -INFINITY, l = 0.f;
     bool ok = run;
     if (ok) {
-      // this row's first two Q pieces into TMEM (lane = row): rows past the tensor read as zero
+      // Q piece hf of this row into TMEM (lane = row): rows past the tensor read as zero
       const int64_t grow = ((int64_t)b * prm.Hq + h) * prm.S + (int64_t)p * L + q_local;
-      const uint32_t tm_q = tmem + lane_base + COL_Q;
-#pragma unroll 1
-      for (int a = 0; a < 2; ++a) {
-        uint32_t w[QW];
-        if (grow < prm.q_rows) {
-          const uint4* src = reinterpret_cast<const uint4*>(prm.q_pieces + ((int64_t)a * prm.q_rows + grow) * QW);
+      uint32_t w[QW];
+      if (grow < prm.q_rows) {
+        const uint4* src = reinterpret_cast<const uint4*>(prm.q_pieces + ((int64_t)hf * prm.q_rows + grow) * QW);
 #pragma unroll
-          for (int i = 0; i < QW / 4; ++i) {
-            const uint4 v = __ldg(src + i);
-            w[4 * i] = v.x;
-            w[4 * i + 1] = v.y;
-            w[4 * i + 2] = v.z;
-            w[4 * i + 3] = v.w;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < QW; ++i) w[i] = 0u;
+        for (int i = 0; i < QW / 4; ++i) {
+          const uint4 v = __ldg(src + i);
+          w[4 * i] = v.x;
+          w[4 * i + 1] = v.y;
+          w[4 * i + 2] = v.z;
+          w[4 * i + 3] = v.w;
         }
+      } else {
 #pragma unroll
-        for (int c = 0; c < QW; c += 32) tmem_st32(tm_q + (uint32_t)(a * QW + c), w + c);
+        for (int i = 0; i < QW; ++i) w[i] = 0u;
       }
+#pragma unroll
+      for (int c = 0; c < QW; c += 32) tmem_st32(tmem + lane_base + COL_Q + (uint32_t)(hf * QW + c), w + c);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -218,24 +237,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int j = 0; j < NB && ok; ++j) {
       int kp, kbk;
       block_at(j, kp, kbk);
-      // visible keys of this row in the block: [0, hi)
+      // visible keys of this row in the block: [0, hi); this warp holds keys [32 hf, 32 hf + 32)
       int hi = (int)min((int64_t)BN, L - (int64_t)kbk * BN);
       if (prm.causal && kp == p) hi = (int)min((int64_t)hi, q_local - (int64_t)kbk * BN + 1);
+      const int lim = hi - 32 * hf;
       ok = mbar_wait(bar(Ly::B_SFULL + (j & 1)), (uint32_t)((j >> 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
                      ROLE_SOFTMAX, j);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      float s[BN];
+      float s[32];
       tmem_ld32(tm_s + 64u * (uint32_t)(j & 1), s);
-      tmem_ld32(tm_s + 64u * (uint32_t)(j & 1) + 32u, s + 32);
       tc_wait_ld();
-      float mb = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        s[c] = (c < hi) ? s[c] * prm.scale_log2 : -INFINITY;
-        mb = fmaxf(mb, s[c]);
+      for (int c = 0; c < 32; ++c) s[c] = (c < lim) ? s[c] * prm.scale_log2 : -INFINITY;
+      float mc0 = max3f(s[0], s[1], s[2]), mc1 = max3f(s[16], s[17], s[18]);
+#pragma unroll
+      for (int c = 3; c + 1 < 16; c += 2) {
+        mc0 = max3f(mc0, s[c], s[c + 1]);
+        mc1 = max3f(mc1, s[16 + c], s[16 + c + 1]);
       }
+      const float mh = max3f(mc0, mc1, fmaxf(s[15], s[31]));
+      // swap half-row maxima with the quadrant's other warp (slot j % 2; the barrier cannot run a
+      // phase ahead: the other warp's next arrival follows its wait on this phase, which needs
+      // this warp's arrival)
+      xch[(j & 1) * 64 + hf * 32 + lane] = mh;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xbar);
+      ok = mbar_wait(xbar, (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_SOFTMAX, j);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const float mb = fmaxf(mh, xch[(j & 1) * 64 + (1 - hf) * 32 + lane]);
       // reference m: set by the first visible block, raised only when the maximum grows by more
       // than 2^LOG2_RESCALE (then O and l are rescaled); P = 2^(s - m) <= 2^LOG2_RESCALE
       float factor = 1.f;
@@ -259,7 +291,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         pv_done = true;
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
+        for (int c = 0; c < D / 2; c += 32) {
           float o[32];
           tmem_ld32(tm_o + (uint32_t)c, o);
           tc_wait_ld();
@@ -269,12 +301,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_st32(tm_o + (uint32_t)c, w);
         }
       }
-      float sum = 0.f;
-      uint32_t p1[BN / 2], p2[BN / 2], p3[BN / 2];
+      uint32_t p1[16], p2[16], p3[16];
+      uint64_t acc2[2] = {0ull, 0ull};
+      const uint64_t nm2 = f2_pack(-mref, -mref);
 #pragma unroll
-      for (int c = 0; c < BN; c += 2) {
-        const float e0 = fast_exp2(s[c] - mref), e1 = fast_exp2(s[c + 1] - mref);
-        sum += e0 + e1;
+      for (int c = 0; c < 32; c += 2) {
+        float x0, x1;
+        f2_unpack(f2_add(f2_pack(s[c], s[c + 1]), nm2), x0, x1);
+        const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+        acc2[(c >> 1) & 1] = f2_add(acc2[(c >> 1) & 1], f2_pack(e0, e1));
         // exact three-piece split of each probability by truncation: x1 = x with the low 16 bits
         // cleared (its top 8 significant bits), r = x - x1 (exact, at most 16 significant bits),
         // x2 = r truncated the same way, x3 = r - x2 (at most 8 significant bits, so a bf16); each
@@ -287,7 +322,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         p2[c / 2] = __byte_perm(w0, w1, 0x7632u);
         p3[c / 2] = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x7632u);
       }
-      l = l * factor + sum;
+      float sa, sb2;
+      f2_unpack(f2_add(acc2[0], acc2[1]), sa, sb2);
+      l = l * factor + (sa + sb2);
       if (!pv_done) {
         ok = mbar_wait(bar(Ly::B_PVDONE), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
                        ROLE_SOFTMAX, j);
@@ -295,14 +332,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
         tc_fence_after();
       }
-      const uint32_t tm_p = tmem + lane_base + COL_P;
-      tmem_st32(tm_p, p1);
-      tmem_st32(tm_p + 32u, p2);
-      tmem_st32(tm_p + 64u, p3);
+      // this warp's 32 keys are packed columns [16 hf, 16 hf + 16) of each piece
+      const uint32_t tm_p = tmem + lane_base + COL_P + 16u * (uint32_t)hf;
+      tmem_st16(tm_p, p1);
+      tmem_st16(tm_p + 32u, p2);
+      tmem_st16(tm_p + 64u, p3);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(Ly::B_PFULL));
+    }
+    if (ok) {
+      // the row's sum: both halves, swapped through the next phase of the quadrant's barrier
+      xch[(NB & 1) * 64 + hf * 32 + lane] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xbar);
+      ok = mbar_wait(xbar, (uint32_t)(NB & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_SOFTMAX, -1);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) l += xch[(NB & 1) * 64 + (1 - hf) * 32 + lane];
     }
     if (ok) {
       ok = mbar_wait(bar(Ly::B_OFULL), 0u, prm.wait_limit_ns, abort_flag, prm.status, ROLE_SOFTMAX, -1);
@@ -313,18 +360,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int64_t prow = (((int64_t)b * prm.Hq + h) * prm.n_slots + it.slot) * L + q_local;
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
+      for (int c = 0; c < D / 2; c += 32) {
         float o[32];
         tmem_ld32(tm_o + (uint32_t)c, o);
         tc_wait_ld();
         if (q_local < L) {
-          float4* dst = reinterpret_cast<float4*>(prm.part_o + prow * D + c);
+          float4* dst = reinterpret_cast<float4*>(prm.part_o + prow * D + hf * (D / 2) + c);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             dst[e] = make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
         }
       }
-      if (q_local < L) prm.part_lse[prow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      if (q_local < L && hf == 0)
+        prm.part_lse[prow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
   } else if (warp == WARP_MMA) {
     // ================================================================ MMA issuer
