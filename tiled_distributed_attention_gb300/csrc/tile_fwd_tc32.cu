@@ -22,7 +22,7 @@
 //     mbarrier), warp 8 MMA issuer (elected lane of a converged warp), warp 9 TMA producer.  Q's first two pieces sit in TMEM, written there by
 //     the softmax warps at the start of the unit, and are the A operand of five of the six S
 //     products, which then read only K from shared memory; shared memory holds Q's third piece,
-//     two stages of K's three pieces and one of V's (32 + 96 + 48 KB at d = 128), 64 keys a
+//     two stages each of K's and V's three pieces (32 + 96 + 96 KB at d = 128), 64 keys a
 //     block.  TMEM: S of even blocks (64 columns) | S of odd blocks (64) | P (three packed bf16
 //     pieces, 96) | O (d) | Q1, Q2 (d / 2 each, packed pairs).  Issue order S(0), S(1), then per
 //     block PV(j), S(j+2): with S double-buffered and P in its own columns, the S products of the
@@ -87,12 +87,12 @@ struct Layout {
   static constexpr uint32_t KP = BN * D * 2;    // one piece of a K or V block
   static constexpr uint32_t QBOX = BM * 128;    // 128 rows x 64 bf16 columns
   static constexpr uint32_t KBOX = BN * 128;    // 64 rows x 64 bf16 columns
-  // Q's third piece (the first two live in TMEM), two K stages, one V stage
+  // Q's third piece (the first two live in TMEM), two K stages, two V stages
   static constexpr uint32_t KSTAGE = 3 * KP;
   static constexpr uint32_t Q_OFF = 0, K_OFF = QP, V_OFF = K_OFF + 2 * KSTAGE;
-  static constexpr uint32_t BAR_OFF = V_OFF + 3 * KP;
-  static constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 3, B_VFULL = 5, B_VEMPTY = 6, B_SFULL = 7, B_PFULL = 9,
-                       B_OFULL = 10, B_DRAIN = 11, B_PVDONE = 12, B_QTMEM = 13, B_XCH = 14, NBARS = 18;
+  static constexpr uint32_t BAR_OFF = V_OFF + 2 * KSTAGE;
+  static constexpr int B_QFULL = 0, B_KFULL = 1, B_KEMPTY = 3, B_VFULL = 5, B_VEMPTY = 7, B_SFULL = 9, B_PFULL = 11,
+                       B_OFULL = 12, B_DRAIN = 13, B_PVDONE = 14, B_QTMEM = 15, B_XCH = 16, NBARS = 20;
   static constexpr uint32_t MISC_OFF = BAR_OFF + NBARS * 8;
   // the two softmax warps of a lane quadrant swap their half-row maxima (and at the end their
   // sums) here: [quadrant 4][phase parity 2][half 2][32 rows] floats
@@ -160,8 +160,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     mbar_init(bar(Ly::B_QTMEM), N_SOFTMAX_WARPS);  // one lane of each softmax warp
     for (int q = 0; q < 4; ++q) mbar_init(bar(Ly::B_XCH + q), 2);  // the quadrant's two warps
-    mbar_init(bar(Ly::B_VFULL), 1);
-    mbar_init(bar(Ly::B_VEMPTY), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(Ly::B_VFULL + s), 1);
+      mbar_init(bar(Ly::B_VEMPTY + s), 1);
+    }
     mbar_init(bar(Ly::B_SFULL), 1);  // one per S buffer
     mbar_init(bar(Ly::B_SFULL + 1), 1);
     mbar_init(bar(Ly::B_PFULL), N_SOFTMAX_WARPS);  // one lane of each softmax warp
@@ -422,21 +424,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int j = 0; j < NB && ok; ++j) {
       ok = mbar_wait_warp(bar(Ly::B_PFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA, j);
       if (ok)
-        ok = mbar_wait_warp(bar(Ly::B_VFULL), (uint32_t)(j & 1), prm.wait_limit_ns, abort_flag, prm.status, ROLE_MMA,
-                            j);
+        ok = mbar_wait_warp(bar(Ly::B_VFULL + (j & 1)), (uint32_t)((j >> 1) & 1), prm.wait_limit_ns, abort_flag,
+                            prm.status, ROLE_MMA, j);
       if (!ok) break;
       tc_fence_after();
       // O += P V over the six piece pairs; P's pieces from TMEM, V's MN-major from shared memory
       const uint32_t pbuf = tmem + COL_P;
       for (int pr = 0; pr < NPAIR; ++pr) {
         const uint32_t pa = pbuf + 32u * (uint32_t)pair_a(pr);
-        const uint64_t vd = v0 + (uint64_t)pair_b(pr) * (Ly::KP >> 4);
+        const uint64_t vd = v0 + (uint64_t)(j & 1) * (Ly::KSTAGE >> 4) + (uint64_t)pair_b(pr) * (Ly::KP >> 4);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           tc_mma_ts_warp(tmem + COL_O, pa + (uint32_t)(kk * 8), vd + (uint64_t)(kk * 128), idesc_pv,
                          (j > 0 || pr > 0 || kk > 0) ? 1u : 0u);
       }
-      tc_commit_warp(bar(Ly::B_VEMPTY));  // V(j) free once these products complete
+      tc_commit_warp(bar(Ly::B_VEMPTY + (j & 1)));  // V(j)'s stage free once these products complete
       tc_commit_warp(bar(Ly::B_PVDONE));  // O holds PV(0..j) and P is free for block j+1
       // the softmax read S(j) before it wrote P(j), so S(j+2) may overwrite S buffer j % 2
       if (j + 2 < NB) ok = issue_s(j + 2);
@@ -456,9 +458,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     bar(Ly::B_QFULL));
     }
     const int64_t kvbase = ((int64_t)b * prm.Hkv + hk) * prm.S;
-    // Two K stages and one V stage.  Products run S(j), PV(j-1), S(j+1), PV(j), ...; K(j) takes the
-    // stage S(j-2) frees, V(j) the one PV(j-1) frees: loads go K(0), K(1), V(0), then K(j), V(j-1)
-    // for j >= 2, then the last V.
+    // Two K stages and two V stages.  Products run S(0), S(1), PV(0), S(2), PV(1), S(3), ...; K(j)
+    // takes the stage S(j-2) frees and V(j) the one PV(j-2) frees, so the loads follow the
+    // products' completion order: K(0), K(1), V(0), V(1), K(2), then K(j), V(j-1) for j >= 3, then
+    // the last V.
     auto load_pieces = [&](const CUtensorMap* tm, uint32_t off, int64_t krow, uint32_t fullbar) {
       mbar_expect_tx(fullbar, 3 * Ly::KP);
       for (int a = 0; a < 3; ++a)
@@ -491,25 +494,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto load_v = [&](int j) -> bool {
       int64_t krow;
       if (!row_of(j, krow)) return false;
-      if (j > 0 && !mbar_wait(bar(Ly::B_VEMPTY), (uint32_t)((j - 1) & 1), prm.wait_limit_ns, abort_flag, prm.status,
-                              ROLE_LOAD, j))
+      const int vs = j & 1;
+      if (j >= 2 && !mbar_wait(bar(Ly::B_VEMPTY + vs), (uint32_t)(((j - 2) >> 1) & 1), prm.wait_limit_ns, abort_flag,
+                               prm.status, ROLE_LOAD, j))
         return false;
-      load_pieces(&tmV, Ly::V_OFF, krow, bar(Ly::B_VFULL));
+      load_pieces(&tmV, Ly::V_OFF + (uint32_t)vs * Ly::KSTAGE, krow, bar(Ly::B_VFULL + vs));
       ++issued_v;
       return true;
     };
     if (ok) ok = load_k(0);
     if (ok && NB > 1) ok = load_k(1);
     if (ok) ok = load_v(0);
-    for (int j = 2; j < NB && ok; ++j) {
+    if (ok && NB > 1) ok = load_v(1);
+    if (ok && NB > 2) ok = load_k(2);
+    for (int j = 3; j < NB && ok; ++j) {
       ok = load_k(j);
       if (ok) ok = load_v(j - 1);
     }
-    if (ok && NB >= 2) ok = load_v(NB - 1);
+    if (ok && NB > 2) ok = load_v(NB - 1);
     if (run && NB > 0) mbar_drain(bar(Ly::B_QFULL), 0u, DRAIN_NS);
     for (int jj = (issued_k > 2 ? issued_k - 2 : 0); jj < issued_k; ++jj)
       mbar_drain(bar(Ly::B_KFULL + (jj & 1)), (uint32_t)((jj >> 1) & 1), DRAIN_NS);
-    if (issued_v > 0) mbar_drain(bar(Ly::B_VFULL), (uint32_t)((issued_v - 1) & 1), DRAIN_NS);
+    for (int jj = (issued_v > 2 ? issued_v - 2 : 0); jj < issued_v; ++jj)
+      mbar_drain(bar(Ly::B_VFULL + (jj & 1)), (uint32_t)((jj >> 1) & 1), DRAIN_NS);
   }
 
   tc_fence_before();
