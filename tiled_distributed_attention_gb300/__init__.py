@@ -436,3 +436,35 @@ def mesh_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, ca
     if return_partials:
         return O, LSE, po, pl
     return O, LSE
+
+
+class MeshAttentionFunction(torch.autograd.Function):
+    """torch.autograd binding of the two public calls: the forward runs mesh_attention and keeps
+    q, k, v, O and LSE; the backward runs mesh_attention_backward with the incoming dO.  Gradients
+    reach q, k and v; LSE is returned as a non-differentiable output (no gradient flows through
+    it).  Argument marshalling only: every step runs in the library's kernels."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, P, causal, kvr, greedy, scale):
+        plan = mesh_attn_plan_create(q.shape[2], P, causal, kvr, greedy)
+        O, LSE = mesh_attention(q, k, v, P, causal, kvr, greedy, scale, plan=plan)
+        ctx.save_for_backward(q, k, v, O, LSE)
+        ctx.plan = plan
+        ctx.args = (P, causal, kvr, greedy, scale)
+        ctx.mark_non_differentiable(LSE)
+        return O, LSE
+
+    @staticmethod
+    def backward(ctx, dO, dLSE):
+        q, k, v, O, LSE = ctx.saved_tensors
+        P, causal, kvr, greedy, scale = ctx.args
+        dQ, dK, dV = mesh_attention_backward(q, k, v, O, LSE, dO.contiguous(), P, causal, kvr, greedy, scale,
+                                             plan=ctx.plan)
+        return dQ, dK, dV, None, None, None, None, None
+
+
+def mesh_attention_autograd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, P: int, causal: bool,
+                            kvr: bool = True, greedy: bool = True, scale: Optional[float] = None):
+    """mesh_attention with autograd: returns (O, LSE); O.backward(...) fills q.grad, k.grad and v.grad
+    through the tile backward."""
+    return MeshAttentionFunction.apply(q, k, v, P, causal, kvr, greedy, scale)
