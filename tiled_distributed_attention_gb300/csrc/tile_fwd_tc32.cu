@@ -124,11 +124,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + Ly::MISC_OFF + 4);
   const int64_t L = prm.L;
 
+  // Units are numbered KV-head-major: (batch, KV head, work item in launch order, query head of
+  // the group, query tile), so the CTAs resident together share one KV head's partitions in L2.
   int64_t uu = blockIdx.x;
+  const int g = prm.Hq / prm.Hkv;
   const int qt = (int)(uu % prm.nqt); uu /= prm.nqt;
-  const int h = (int)(uu % prm.Hq); uu /= prm.Hq;
-  const int b = (int)(uu % prm.B);
-  const int idx = (int)(uu / prm.B);
+  const int gi = (int)(uu % g); uu /= g;
+  const int idx = (int)(uu % prm.n_items); uu /= prm.n_items;
+  const int h = (int)(uu % prm.Hkv) * g + gi;
+  const int b = (int)(uu / prm.Hkv);
   const DevItem it = prm.items[idx];
   const bool unit_ok = it.p >= 0 && it.p < prm.P && it.slot >= 0 && it.slot < prm.n_slots && it.n_kv >= 1 &&
                        it.kv_off >= 0;
