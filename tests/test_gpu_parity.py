@@ -78,6 +78,23 @@ def test_growing_and_shrinking_scores(lib, ramp, causal):
     check_partials(lib, w, plan, po, pl, q, k, v)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("ramp", [6.0, -0.9])
+def test_growing_and_shrinking_scores_f32(lib, ramp, causal):
+    """The same ramps with fp32 inputs, at the fp32 tolerance and with V unscaled: the growing
+    ramp raises the running reference (and rescales O and l) many times per unit, which in the
+    fp32 kernel the two softmax warps of each row decide together from their swapped half-row
+    maxima, each rescaling its half of O.  Scores reach ~35 here, so fp32 accumulation of the
+    score's 768 piece products is what the LSE error measures (about 1e-5)."""
+    w = Workload(118, "f32_ramp", 1, 2, 1, 4096, 128, "f32", causal, 4)
+    q, k, v = make_qkv(w)
+    ramp_k = 1.0 + ramp * torch.arange(w.S, dtype=torch.float32) / w.S
+    k = k * ramp_k[None, None, :, None]
+    O, LSE, po, pl, plan = run_gpu(lib, w, q, k, v)
+    check_full(w, O, LSE, q, k, v)
+    check_partials(lib, w, plan, po, pl, q, k, v)
+
+
 def test_closed_forms_on_gpu(lib):
     """Constant V gives O = V; causal row 0 gives O_0 = V_0 and LSE_0 = scale q_0 . k_0; equal
     keys give the mean of the visible values and LSE = ln(count) + score."""

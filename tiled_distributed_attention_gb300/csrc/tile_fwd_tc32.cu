@@ -53,9 +53,12 @@ constexpr int NPAIR = 6;
 constexpr int64_t DRAIN_NS = 200000000;
 constexpr int ROLE_SOFTMAX = 1, ROLE_MMA = 2, ROLE_LOAD = 3, ROLE_ITEM = 4;
 
-// piece pairs (a, b) of a product: x_a y_b
-__device__ __forceinline__ int pair_a(int i) { return i == 2 ? 1 : i == 4 ? 2 : i == 5 ? 1 : 0; }
-__device__ __forceinline__ int pair_b(int i) { return i == 1 ? 1 : i == 3 ? 2 : i == 5 ? 1 : 0; }
+// piece pairs (a, b) of a product, x_a y_b, smallest first: (1,1), (2,0), (0,2), (1,0), (0,1),
+// (0,0).  S starts from a zero accumulator every block, so its terms of order 2^-16 and 2^-8 are
+// summed at their own magnitude before the leading term is added, instead of each being rounded
+// to the leading term's precision.
+__device__ __forceinline__ int pair_a(int i) { return i == 0 ? 1 : i == 1 ? 2 : i == 3 ? 1 : 0; }
+__device__ __forceinline__ int pair_b(int i) { return i == 0 ? 1 : i == 2 ? 2 : i == 4 ? 1 : 0; }
 
 struct Params {
   const DevItem* items;
