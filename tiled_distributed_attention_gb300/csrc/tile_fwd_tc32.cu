@@ -19,18 +19,18 @@
 //   tile_fwd_tc32_kernel: one CTA per (work item, batch, head, 128-row query tile); 10 warps --
 //     warps 0-7 softmax (two per TMEM lane quadrant: one thread per row, each warp 32 of a
 //     block's 64 keys, the pair swapping half-row maxima through shared memory and a bounded
-//     mbarrier), warp 8 MMA issuer (elected lane of a converged warp), warp 9 TMA producer.  Q's first two pieces sit in TMEM, written there by
-//     the softmax warps at the start of the unit, and are the A operand of five of the six S
-//     products, which then read only K from shared memory; shared memory holds Q's third piece,
-//     two stages each of K's and V's three pieces (32 + 96 + 96 KB at d = 128), 64 keys a
-//     block.  TMEM: S of even blocks (64 columns) | S of odd blocks (64) | P (three packed bf16
-//     pieces, 96) | O (d) | Q1, Q2 (d / 2 each, packed pairs).  Issue order S(0), S(1), then per
-//     block PV(j), S(j+2): with S double-buffered and P in its own columns, the S products of the
-//     next block run while the softmax works on this one, so the tensor pipe does not wait for
-//     the softmax between S and PV.  The softmax stores P(j) once PV(j-1) has completed.  It
-//     takes the block maximum every block but raises its reference (and rescales O and l) only
-//     when the maximum grew by more than 2^8; the exact three-piece split keeps P's full fp32
-//     value at any magnitude up to that bound.
+//     mbarrier), warp 8 MMA issuer (elected lane of a converged warp), warp 9 TMA producer.
+//     Q's first two pieces sit in TMEM, written there by the softmax warps at the start of the
+//     unit, and are the A operand of five of the six S products, which then read only K from
+//     shared memory; shared memory holds Q's third piece and two stages each of K's and V's
+//     three pieces (32 + 96 + 96 KB at d = 128), 64 keys a block.  TMEM: S of even blocks (64
+//     columns) | S of odd blocks (64) | P (three packed bf16 pieces, 96) | O (d) | Q1, Q2 (d / 2
+//     each, packed pairs).  Issue order S(0), S(1), then per block PV(j), S(j+2): with S
+//     double-buffered and P in its own columns, the S products of the next block run while the
+//     softmax works on this one.  The softmax stores P(j) once PV(j-1) has completed.  It takes
+//     the block maximum every block but raises its reference (and rescales O and l) only when the
+//     maximum grew by more than 2^8; the exact three-piece split keeps P's full fp32 value at any
+//     magnitude up to that bound.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const bool unit_ok = it.p >= 0 && it.p < prm.P && it.slot >= 0 && it.slot < prm.n_slots && it.n_kv >= 1 &&
                        it.kv_off >= 0;
   const int p = it.p;
-  const int hk = h / (prm.Hq / prm.Hkv);
+  const int hk = h / g;
   int NB = 0;
   if (unit_ok)
     for (int ki = 0; ki < it.n_kv; ++ki) NB += kblocks(__ldg(prm.kv_list + it.kv_off + ki), p, prm.causal, prm.nb, qt);
