@@ -33,6 +33,12 @@ SMALL = [
     Workload(114, "bf16_mqa_32_heads", 1, 32, 1, 1024, 128, "bf16", True, 4),
     Workload(115, "f32_gqa_d64", 1, 4, 2, 765, 64, "f32", False, 9),
     Workload(116, "bf16_noncausal_d64_L1000", 1, 2, 1, 4000, 64, "bf16", False, 4),
+    # fp32 inputs through the same edge cases: batch, GQA and ragged partitions together; MQA at
+    # d = 64; partitions of 8 and of 1 token, where one softmax warp of each row holds no key
+    Workload(119, "f32_batch2_gqa_ragged_causal", 2, 4, 2, 800, 128, "f32", True, 4),
+    Workload(120, "f32_mqa_8_heads_d64", 1, 8, 1, 1024, 64, "f32", True, 4),
+    Workload(121, "f32_tiny_partitions_L8", 1, 2, 2, 512, 128, "f32", True, 64),
+    Workload(122, "f32_one_token_partitions", 1, 2, 1, 16, 128, "f32", True, 16),
 ]
 
 
