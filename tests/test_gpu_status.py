@@ -15,13 +15,16 @@ from tests.gpu_helpers import check_full
 pytestmark = pytest.mark.gpu
 
 
-def test_wait_timeout_reports_status_and_context_survives(lib):
-    w = Workload(120, "status", 1, 2, 1, 2048, 128, "bf16", True, 4)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_wait_timeout_reports_status_and_context_survives(lib, dtype):
+    """Both forward kernels; in the fp32 one the waits include the per-block swap of half-row
+    maxima between the two softmax warps of a row, which must give up as the others do."""
+    w = Workload(120, "status", 1, 2, 1, 2048, 128, dtype, True, 4)
     q, k, v = make_qkv(w)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     plan = lib.mesh_attn_plan_create(w.S, w.P, w.causal, True, True)
     po, pl = lib.new_partials(plan, 1, 2, 128)
-    ws = lib.new_workspace(plan)
+    ws = lib.new_workspace(plan, "cuda", qd, kd)
     st = lib.new_status()
     O = torch.full_like(qd, 7.0)
     LSE = torch.full((1, 2, w.S), 7.0, device="cuda")
