@@ -75,6 +75,10 @@ WORKLOADS: Dict[str, Workload] = {
     # so that a replayed counter capture holds about 4 GB on the device
     "stress_64k": Workload(6, "stress_64k", 1, 8, 2, 65536, 128, "bf16", True, 256,
                            k_scale=4.0, sampled_rows=4096),
+    # the 1M-token sequence length the pages measure across GPUs, on one GPU: 8 query heads and
+    # 2 KV heads so that its fp32 partials (32,272 slots of 1,024 rows, 136 GB) fit in HBM
+    "long_1m_causal": Workload(7, "long_1m_causal", 1, 8, 2, 1048576, 128, "bf16", True, 1024,
+                               sampled_rows=1024),
 }
 
 

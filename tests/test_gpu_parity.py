@@ -123,7 +123,7 @@ def test_closed_forms_on_gpu(lib):
         assert max_err(LSE[0, h], torch.log(torch.arange(1, 1025, dtype=torch.float64)) + s[h]) <= 1e-3
 
 
-FULL = ["bf16_causal_16k", "gqa_causal_64k", "long_128k", "long_128k_causal", "stress_256k"]
+FULL = ["bf16_causal_16k", "gqa_causal_64k", "long_128k", "long_128k_causal", "stress_256k", "long_1m_causal"]
 
 
 @pytest.mark.parametrize("name", FULL)
